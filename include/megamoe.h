@@ -1,0 +1,186 @@
+/*
+ * megamoe.h -- C ABI of the GB300 (sm_103a) fused MoE layer forward, a8w4.
+ *
+ * One call runs a whole routed-expert MoE layer on one GPU: sigmoid top-k
+ * routing, the fused EPLB logical->physical remap with per-expert load
+ * recording, MXFP8 activation quantisation, dispatch into expert-sorted
+ * tiles, GEMM1 (gate/up) with a SwiGLU + MXFP8 requantisation epilogue,
+ * GEMM2 (down) and the top-k weighted combine.  Sources for the operation:
+ *   - "sglang PR #47065" (Title/switches, Modifications): the operator is
+ *     one kernel for "quant, dispatch, GEMM1, GEMM2 and combine", with a
+ *     small-input path (up to 512 tokens) and a persistent large-input path
+ *     (>= 1024 tokens), a per-layer slot (bind_layer) and a three-state
+ *     large-input switch;
+ *   - "sglang PR #35619" (Summary, EPLB arm settings): fused EPLB remap and
+ *     per-expert load recording, enabled for prefill only, and graph-safe
+ *     handling of an idle batch;
+ *   - "InferenceX PR #3430" (draft-precision notes): routed experts are MXFP4
+ *     and the MoE runs a8w4.
+ * On one GPU the pages' cross-rank dispatch/combine is a local permute and a
+ * local gather.
+ *
+ * Conventions for every call:
+ *   - every function returns an mm_status; nothing throws or aborts;
+ *   - a handle is not thread-safe; use it from one host thread and, for
+ *     mm_forward, one stream at a time;
+ *   - "device pointer" means memory of the handle's device (cudaMalloc or
+ *     torch CUDA tensors); "host pointer" means ordinary CPU memory;
+ *   - the library never takes ownership of caller memory.
+ *
+ * Formats:
+ *   bf16      IEEE bfloat16, little endian
+ *   MXFP4     OCP Microscaling v1.0: e2m1 elements, two per byte, element 2i
+ *             in the low nibble of byte i; one e8m0 scale byte per 32
+ *             consecutive elements along the reduction (K) axis
+ *   MXFP8     e4m3 elements, one e8m0 scale byte per 32 along K
+ */
+#ifndef MEGAMOE_H
+#define MEGAMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MM_API __attribute__((visibility("default")))
+#else
+#define MM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mm_ctx *mm_handle;
+typedef struct CUstream_st *mm_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    MM_OK = 0,
+    MM_ERR_INVALID_ARG = 1, /* null pointer, bad value or misaligned pointer */
+    MM_ERR_UNSUPPORTED = 2, /* shape outside the supported set, or no sm_103 GPU */
+    MM_ERR_NOT_READY = 3,   /* weights (or, when P > E, the EPLB map) not set */
+    MM_ERR_CAPACITY = 4,    /* tokens above mm_reserve, or forced small path above its limit */
+    MM_ERR_CUDA = 5,        /* a CUDA runtime call failed (allocation, copy, launch) */
+    MM_ERR_TIMEOUT = 6,     /* a device-side wait gave up (latched, see mm_get_status) */
+    MM_ERR_DEVICE = 7       /* a device-side check failed (latched, see mm_get_status) */
+} mm_status;
+
+typedef enum {
+    MM_ROUTE_AUTO = 0,  /* T <= small limit (512): small path; otherwise large path */
+    MM_ROUTE_SMALL = 1, /* always the small path; T above its limit -> MM_ERR_CAPACITY */
+    MM_ROUTE_LARGE = 2  /* always the large path */
+} mm_route;
+
+#define MM_MAX_LAYERS 256
+#define MM_MAX_EXPERTS 512
+#define MM_MAX_TOPK 8
+
+/* Create a layer operator.  num_experts E (logical), num_physical P >= E
+ * (physical slots; P - E redundant replicas), topk k, hidden H, inter I.
+ * Supported: 1 <= k <= min(E, 8), E <= 512, P <= 512, H % 128 == 0,
+ * I % 128 == 0, H <= 16384, I <= 8192; otherwise MM_ERR_UNSUPPORTED.
+ * Uses the current CUDA device, which must be sm_103.  Allocates the
+ * per-layer count table; weights and workspace come later.  The environment
+ * variables MM_SMALL_M_MAX (default 512) and MM_LARGE_M_MIN (default 1024)
+ * are read here, once. */
+MM_API mm_status mm_create(int num_experts, int num_physical, int topk, int hidden, int inter,
+                    mm_handle *out);
+
+/* Free everything the handle owns.  Waits for the device.  NULL is a no-op. */
+MM_API mm_status mm_destroy(mm_handle h);
+
+/* Expert weights, indexed by physical expert (device pointers, 32-byte
+ * aligned):
+ *   w1       [P, 2I, H/2]  MXFP4 elements; rows 0..I-1 gate, I..2I-1 up
+ *   w1_scale [P, 2I, H/32] e8m0
+ *   w2       [P, H, I/2]   MXFP4 elements
+ *   w2_scale [P, H, I/32]  e8m0
+ * Copied (scales re-laid out for the tensor cores) into library-owned
+ * memory; the caller may free its buffers after return.  Synchronous.  Not
+ * allowed during stream capture. */
+MM_API mm_status mm_set_weights(mm_handle h, const uint8_t *w1, const uint8_t *w1_scale,
+                         const uint8_t *w2, const uint8_t *w2_scale);
+
+/* EPLB map (host pointers): phys_of_logical [E, max_replicas] row-major,
+ * replica_counts [E].  Entries of row e beyond replica_counts[e] are ignored.
+ * Valid iff 1 <= replica_counts[e] <= max_replicas and every physical id
+ * 0..P-1 appears exactly once among the used entries; otherwise
+ * MM_ERR_INVALID_ARG and the previous map stays.  A (token t, slot j) pair
+ * routed to logical e goes to phys_of_logical[e][(t + j) % replica_counts[e]]
+ * ("sglang PR #35619", fused EPLB remap).  When P == E the identity map is
+ * the default; when P > E, mm_forward returns MM_ERR_NOT_READY until a map is
+ * set.  Synchronous; not allowed during stream capture. */
+MM_API mm_status mm_set_eplb_map(mm_handle h, const int32_t *phys_of_logical,
+                          const int32_t *replica_counts, int max_replicas);
+
+/* Select the count slot that later forwards record into (the pages' per-layer
+ * protocol slot, "sglang PR #47065", Modifications).  0 <= layer < 256. */
+MM_API mm_status mm_bind_layer(mm_handle h, int layer);
+
+/* Per-logical-expert load recording for later forwards: on != 0 enables it.
+ * Off by default; the pages enable it for prefill steps only, which is the
+ * caller's choice here ("sglang PR #35619", EPLB arm settings). */
+MM_API mm_status mm_set_recording(mm_handle h, int on);
+
+/* Route selection for later forwards (three-state analogue of the pages'
+ * set_large_m_enabled, "sglang PR #47065", aiter commit message). */
+MM_API mm_status mm_set_route(mm_handle h, mm_route route);
+
+/* Reserve workspace for up to max_tokens tokens per forward (the pages' MTPR
+ * capacity).  Allocates; call before any stream capture.  Calling again with
+ * a larger value reallocates (synchronous); a smaller value is a no-op. */
+MM_API mm_status mm_reserve(mm_handle h, int64_t max_tokens);
+
+/* The layer forward.  Device pointers, 16-byte aligned:
+ *   hidden   [T, H] bf16
+ *   logits   [T, E] fp32 router logits (finite)
+ *   bias     [E]    fp32 selection bias, or NULL for zeros
+ *   out      [T, H] bf16, must not overlap any input
+ * num_tokens T >= 0.  Enqueued on `stream`; no host synchronisation and no
+ * allocation, so the call can be captured into a CUDA graph.  T == 0 returns
+ * MM_OK and enqueues nothing (idle batch, "sglang PR #35619", graph-safe idle
+ * handling).  T > reserved capacity -> MM_ERR_CAPACITY, nothing enqueued.
+ * Device-side failures (a wait that timed out) are latched and reported by
+ * mm_get_status and mm_read_counts. */
+MM_API mm_status mm_forward(mm_handle h, const void *hidden, const float *logits, const float *bias,
+                     void *out, int64_t num_tokens, mm_stream stream);
+
+/* Copy the int64 per-logical-expert counts [E] of slot `layer`, accumulated
+ * since creation or the last mm_reset_counts, to host memory out_host.
+ * Synchronises the device first (the only device-to-host read on the path).
+ * Returns the latched device error, if any, after copying. */
+MM_API mm_status mm_read_counts(mm_handle h, int layer, int64_t *out_host);
+
+/* Zero the counts of slot `layer` (-1: every slot).  Synchronous. */
+MM_API mm_status mm_reset_counts(mm_handle h, int layer);
+
+/* Synchronise the device, store the latched device status in *device_code
+ * (0 = none, else an mm_status value) and clear it. */
+MM_API mm_status mm_get_status(mm_handle h, int *device_code);
+
+/* Intermediates of the last forward, for tests.  Synchronous.  `stage`:
+ *   0 idx     int32 [T, k]     logical experts in selection order
+ *   1 weights fp32  [T, k]     normalised routing weights
+ *   2 phys    int32 [T, k]     physical experts
+ *   3 pos     int32 [T, k]     dispatch row of each (token, slot) pair
+ *   4 offsets int32 [P + 1]    start row of each physical expert's segment
+ *                              (segments are padded to 128 rows); [P] = total
+ *   5 xq      uint8 [rows, H]  dispatched MXFP8 activation codes
+ *   6 xs      uint8 [rows, H/32] their scale bytes, row-major
+ *   7 hq      uint8 [rows, I]  GEMM1 output codes (after SwiGLU, requant)
+ *   8 hs      uint8 [rows, I/32] their scale bytes, row-major
+ *   9 y       bf16  [rows, H]  GEMM2 output rows
+ * where rows = offsets[P].  Copies min(bytes, size of the stage) bytes into
+ * dst_host; MM_ERR_INVALID_ARG for an unknown stage. */
+MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t bytes);
+
+/* Size in bytes of a debug stage for the last forward (0 before any). */
+MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);
+
+/* Short text for a status code (static storage). */
+MM_API const char *mm_status_string(mm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEGAMOE_H */

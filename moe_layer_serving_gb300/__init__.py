@@ -1,0 +1,185 @@
+"""Python binding of libmegamoe.so, the GB300 fused a8w4 MoE layer forward.
+
+Argument marshalling only: every stage of the layer runs in the library's
+sm_103a kernels.  The module-level ``mm_*`` functions are the C entry points
+with their C names (see include/megamoe.h); ``MegaMoE`` wraps one handle for
+torch tensors.  There is no fallback: if the library is not built, the first
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+__all__ = ["lib", "MegaMoE", "MegaMoEError", "library_path", "STATUS", "ROUTE_AUTO", "ROUTE_SMALL",
+           "ROUTE_LARGE", "DUMP_STAGES"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmegamoe.so")
+
+STATUS = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_NOT_READY",
+          4: "MM_ERR_CAPACITY", 5: "MM_ERR_CUDA", 6: "MM_ERR_TIMEOUT", 7: "MM_ERR_DEVICE"}
+MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_NOT_READY = 0, 1, 2, 3
+MM_ERR_CAPACITY, MM_ERR_CUDA, MM_ERR_TIMEOUT, MM_ERR_DEVICE = 4, 5, 6, 7
+ROUTE_AUTO, ROUTE_SMALL, ROUTE_LARGE = 0, 1, 2
+# debug stage -> (name, numpy dtype, per-row width: None = flat)
+DUMP_STAGES = {0: ("idx", np.int32), 1: ("weights", np.float32), 2: ("phys", np.int32), 3: ("pos", np.int32),
+               4: ("offsets", np.int32), 5: ("xq", np.uint8), 6: ("xs", np.uint8), 7: ("hq", np.uint8),
+               8: ("hs", np.uint8), 9: ("y", np.uint16)}
+
+_p, _i32, _i64, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
+_SIGS = {
+    "mm_create": [_i32, _i32, _i32, _i32, _i32, C.POINTER(_p)],
+    "mm_destroy": [_p],
+    "mm_set_weights": [_p, _p, _p, _p, _p],
+    "mm_set_eplb_map": [_p, _p, _p, _i32],
+    "mm_bind_layer": [_p, _i32],
+    "mm_set_recording": [_p, _i32],
+    "mm_set_route": [_p, _i32],
+    "mm_reserve": [_p, _i64],
+    "mm_forward": [_p, _p, _p, _p, _p, _i64, _p],
+    "mm_read_counts": [_p, _i32, _p],
+    "mm_reset_counts": [_p, _i32],
+    "mm_get_status": [_p, C.POINTER(_i32)],
+    "mm_debug_dump": [_p, _i32, _p, _sz],
+    "mm_debug_size": [_p, _i32, C.POINTER(_sz)],
+}
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it with "
+                               "moe_layer_serving_gb300.build.build() (needs nvcc, sm_103a)")
+        L = C.CDLL(library_path)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = C.c_int
+        L.mm_status_string.argtypes = [C.c_int]
+        L.mm_status_string.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def _export(name):
+    def call(*args):
+        return getattr(lib(), name)(*args)
+    call.__name__ = name
+    call.__doc__ = f"C entry point {name} (include/megamoe.h)."
+    return call
+
+
+for _n in list(_SIGS) + ["mm_status_string"]:
+    globals()[_n] = _export(_n)
+    __all__.append(_n)
+
+
+class MegaMoEError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def _check(st: int, what: str) -> None:
+    if st != MM_OK:
+        raise MegaMoEError(what, st)
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream  # torch.cuda.Stream
+
+
+class MegaMoE:
+    """One fused MoE layer operator (one handle) on the current CUDA device."""
+
+    def __init__(self, num_experts: int, num_physical: int, topk: int, hidden: int, inter: int):
+        h = C.c_void_p()
+        _check(lib().mm_create(num_experts, num_physical, topk, hidden, inter, C.byref(h)), "mm_create")
+        self._h = h
+        self.E, self.P, self.k, self.H, self.I = num_experts, num_physical, topk, hidden, inter
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self) -> None:
+        if self._h:
+            lib().mm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_weights(self, w1, w1_scale, w2, w2_scale) -> None:
+        _check(lib().mm_set_weights(self._h, _addr(w1), _addr(w1_scale), _addr(w2), _addr(w2_scale)),
+               "mm_set_weights")
+
+    def set_eplb_map(self, phys_of_logical, replica_counts) -> None:
+        m = np.ascontiguousarray(phys_of_logical, np.int32)
+        rc = np.ascontiguousarray(replica_counts, np.int32)
+        _check(lib().mm_set_eplb_map(self._h, m.ctypes.data, rc.ctypes.data, m.shape[1]), "mm_set_eplb_map")
+
+    def bind_layer(self, layer: int) -> None:
+        _check(lib().mm_bind_layer(self._h, layer), "mm_bind_layer")
+
+    def set_recording(self, on: bool) -> None:
+        _check(lib().mm_set_recording(self._h, int(bool(on))), "mm_set_recording")
+
+    def set_route(self, route: int) -> None:
+        _check(lib().mm_set_route(self._h, route), "mm_set_route")
+
+    def reserve(self, max_tokens: int) -> None:
+        _check(lib().mm_reserve(self._h, max_tokens), "mm_reserve")
+
+    def forward(self, hidden, logits, bias, out, num_tokens: int | None = None, stream=None) -> int:
+        """Enqueue one forward; returns the status (raises on failure)."""
+        T = hidden.shape[0] if num_tokens is None else num_tokens
+        st = lib().mm_forward(self._h, _addr(hidden), _addr(logits), _addr(bias), _addr(out), T, _stream(stream))
+        _check(st, "mm_forward")
+        return st
+
+    def read_counts(self, layer: int) -> np.ndarray:
+        out = np.zeros(self.E, np.int64)
+        _check(lib().mm_read_counts(self._h, layer, out.ctypes.data), "mm_read_counts")
+        return out
+
+    def reset_counts(self, layer: int = -1) -> None:
+        _check(lib().mm_reset_counts(self._h, layer), "mm_reset_counts")
+
+    def get_status(self) -> int:
+        code = C.c_int(0)
+        _check(lib().mm_get_status(self._h, C.byref(code)), "mm_get_status")
+        return code.value
+
+    def debug_dump(self, stage: int) -> np.ndarray:
+        n = C.c_size_t(0)
+        _check(lib().mm_debug_size(self._h, stage, C.byref(n)), "mm_debug_size")
+        dtype = DUMP_STAGES[stage][1]
+        buf = np.zeros(n.value // np.dtype(dtype).itemsize, dtype)
+        _check(lib().mm_debug_dump(self._h, stage, buf.ctypes.data, n.value), "mm_debug_dump")
+        return buf

@@ -1,0 +1,450 @@
+// mm_api.cu -- the C ABI of the fused MoE layer: argument checks, owned
+// device memory (weights, EPLB map, per-layer counts, workspace), TMA
+// descriptors, route choice and the launch sequence of one forward.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "mm_internal.h"
+
+using mm::kTile;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D row-major [rows][cols] tensor map, box [box_rows][128 elements], 128-byte swizzle.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t cols, uint64_t rows,
+              uint64_t row_bytes, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int env_int(const char* name, int dflt)
+{
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    char* end = nullptr;
+    long x = strtol(v, &end, 10);
+    return (end && *end == 0 && x >= 0 && x < (1L << 30)) ? static_cast<int>(x) : dflt;
+}
+
+#define CK(call)                                   \
+    do {                                           \
+        if ((call) != cudaSuccess) {               \
+            cudaGetLastError();                    \
+            return MM_ERR_CUDA;                    \
+        }                                          \
+    } while (0)
+
+bool capturing(cudaStream_t s)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
+template <typename T>
+T* carve(uint8_t*& p, size_t n)
+{
+    T* r = reinterpret_cast<T*>(p);
+    p += (n * sizeof(T) + 255) & ~size_t(255);
+    return r;
+}
+
+void free_ws(mm_ctx* c)
+{
+    if (c->ws) cudaFree(c->ws);
+    c->ws = nullptr;
+    c->ws_bytes = 0;
+    c->cap_tokens = 0;
+    c->maps_ws = false;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mm_status_string(mm_status s)
+{
+    switch (s) {
+        case MM_OK: return "ok";
+        case MM_ERR_INVALID_ARG: return "invalid argument";
+        case MM_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case MM_ERR_NOT_READY: return "weights or EPLB map not set";
+        case MM_ERR_CAPACITY: return "token count above capacity";
+        case MM_ERR_CUDA: return "CUDA runtime error";
+        case MM_ERR_TIMEOUT: return "device-side wait timed out";
+        case MM_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
+{
+    if (!out) return MM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (E < 1 || P < E || k < 1 || k > MM_MAX_TOPK || k > E || E > MM_MAX_EXPERTS || P > MM_MAX_EXPERTS ||
+        H < 128 || I < 128 || H % 128 || I % 128 || H > 16384 || I > 8192)
+        return MM_ERR_UNSUPPORTED;
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    CK(cudaGetDeviceProperties(&prop, dev));
+    if (prop.major != 10 || prop.minor != 3) return MM_ERR_UNSUPPORTED;
+    if (!encode_fn()) return MM_ERR_UNSUPPORTED;
+    mm_ctx* c = new (std::nothrow) mm_ctx();
+    if (!c) return MM_ERR_CUDA;
+    c->dev = dev;
+    c->sms = prop.multiProcessorCount;
+    c->E = E;
+    c->P = P;
+    c->k = k;
+    c->H = H;
+    c->I = I;
+    c->small_max = env_int("MM_SMALL_M_MAX", 512);
+    c->large_min = env_int("MM_LARGE_M_MIN", 1024);
+    if (mm::gemm_prepare(dev) != cudaSuccess ||
+        cudaMalloc(&c->counts, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
+        cudaMemset(c->counts, 0, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
+        cudaMalloc(&c->status, sizeof(int)) != cudaSuccess || cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        mm_destroy(c);
+        return MM_ERR_CUDA;
+    }
+    if (P == E) {
+        std::vector<int32_t> m(E), rc(E, 1);
+        for (int e = 0; e < E; ++e) m[e] = e;
+        mm_status st = mm_set_eplb_map(c, m.data(), rc.data(), 1);
+        if (st != MM_OK) {
+            mm_destroy(c);
+            return st;
+        }
+    }
+    *out = c;
+    return MM_OK;
+}
+
+mm_status mm_destroy(mm_handle c)
+{
+    if (!c) return MM_OK;
+    cudaDeviceSynchronize();
+    cudaGetLastError();
+    free_ws(c);
+    void* ptrs[] = {c->w1, c->w1_sf, c->w2, c->w2_sf, c->map, c->rc, c->counts, c->status};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    delete c;
+    return MM_OK;
+}
+
+mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s)
+{
+    if (!c || !w1 || !w1s || !w2 || !w2s) return MM_ERR_INVALID_ARG;
+    if (!aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1s, 16) || !aligned(w2s, 16)) return MM_ERR_INVALID_ARG;
+    if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    const size_t P = c->P, H = c->H, I = c->I;
+    const size_t n_w1 = P * 2 * I * H / 2, n_w1s = P * 2 * I * H / 32;
+    const size_t n_w2 = P * H * I / 2, n_w2s = P * H * I / 32;
+    if (!c->w1) {
+        if (cudaMalloc(&c->w1, n_w1) != cudaSuccess || cudaMalloc(&c->w1_sf, n_w1s) != cudaSuccess ||
+            cudaMalloc(&c->w2, n_w2) != cudaSuccess || cudaMalloc(&c->w2_sf, n_w2s) != cudaSuccess) {
+            cudaGetLastError();
+            return MM_ERR_CUDA;
+        }
+    }
+    CK(cudaMemcpy(c->w1, w1, n_w1, cudaMemcpyDeviceToDevice));
+    CK(cudaMemcpy(c->w2, w2, n_w2, cudaMemcpyDeviceToDevice));
+    CK(mm::launch_tile_scales(w1s, c->w1_sf, static_cast<int64_t>(P * 2 * I), c->H, nullptr));
+    CK(mm::launch_tile_scales(w2s, c->w2_sf, static_cast<int64_t>(P * H), c->I, nullptr));
+    CK(cudaDeviceSynchronize());
+    if (!make_map(&c->maps.w1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, c->w1, H, P * 2 * I, H / 2, kTile) ||
+        !make_map(&c->maps.w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, c->w2, I, P * H, I / 2, kTile))
+        return MM_ERR_CUDA;
+    c->maps_weights = true;
+    c->weights_set = true;
+    return MM_OK;
+}
+
+mm_status mm_set_eplb_map(mm_handle c, const int32_t* pol, const int32_t* rc, int R)
+{
+    if (!c || !pol || !rc || R < 1 || R > c->P) return MM_ERR_INVALID_ARG;
+    std::vector<int> seen(c->P, 0);
+    for (int e = 0; e < c->E; ++e) {
+        if (rc[e] < 1 || rc[e] > R) return MM_ERR_INVALID_ARG;
+        for (int s = 0; s < rc[e]; ++s) {
+            const int p = pol[static_cast<int64_t>(e) * R + s];
+            if (p < 0 || p >= c->P || seen[p]) return MM_ERR_INVALID_ARG;
+            seen[p] = 1;
+        }
+    }
+    for (int p = 0; p < c->P; ++p)
+        if (!seen[p]) return MM_ERR_INVALID_ARG;
+    if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    std::vector<int32_t> m(static_cast<size_t>(c->E) * R);
+    for (int e = 0; e < c->E; ++e)
+        for (int s = 0; s < R; ++s) m[static_cast<size_t>(e) * R + s] = s < rc[e] ? pol[e * R + s] : 0;
+    int32_t *dm = nullptr, *drc = nullptr;
+    if (cudaMalloc(&dm, m.size() * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&drc, c->E * sizeof(int32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        if (dm) cudaFree(dm);
+        return MM_ERR_CUDA;
+    }
+    if (cudaMemcpy(dm, m.data(), m.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(drc, rc, c->E * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(dm);
+        cudaFree(drc);
+        return MM_ERR_CUDA;
+    }
+    cudaDeviceSynchronize();
+    if (c->map) cudaFree(c->map);
+    if (c->rc) cudaFree(c->rc);
+    c->map = dm;
+    c->rc = drc;
+    c->R = R;
+    c->map_set = true;
+    return MM_OK;
+}
+
+mm_status mm_bind_layer(mm_handle c, int layer)
+{
+    if (!c || layer < 0 || layer >= MM_MAX_LAYERS) return MM_ERR_INVALID_ARG;
+    c->layer = layer;
+    return MM_OK;
+}
+
+mm_status mm_set_recording(mm_handle c, int on)
+{
+    if (!c) return MM_ERR_INVALID_ARG;
+    c->recording = on ? 1 : 0;
+    return MM_OK;
+}
+
+mm_status mm_set_route(mm_handle c, mm_route r)
+{
+    if (!c || (r != MM_ROUTE_AUTO && r != MM_ROUTE_SMALL && r != MM_ROUTE_LARGE)) return MM_ERR_INVALID_ARG;
+    c->route = r;
+    return MM_OK;
+}
+
+mm_status mm_reserve(mm_handle c, int64_t max_tokens)
+{
+    if (!c || max_tokens < 0 || max_tokens > (int64_t(1) << 24)) return MM_ERR_INVALID_ARG;
+    if (max_tokens <= c->cap_tokens) return MM_OK;
+    if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    const int64_t npairs = max_tokens * c->k;
+    const int64_t rows = (npairs + static_cast<int64_t>(c->P) * (kTile - 1) + kTile - 1) / kTile * kTile;
+    const int64_t tiles = rows / kTile;
+    const int64_t chunks = (npairs + mm::kChunkPairs - 1) / mm::kChunkPairs;
+    const int64_t H = c->H, I = c->I;
+    // size pass, then carve
+    size_t bytes = 0;
+    auto add = [&](size_t n) { bytes += (n + 255) & ~size_t(255); };
+    add(npairs * 4 * 4);                      // idx, phys, pos, wgt
+    add(chunks * c->P * 4);
+    add((c->P + 1) * 4);
+    add(tiles * 4 * 4 + 4);                   // tile table, done1, num_tiles
+    add(rows * H);
+    add(rows * H / 32);
+    add(rows * I);
+    add(rows * I / 32);
+    add(rows * H * 2);
+    bytes += 8 * 256;
+    cudaDeviceSynchronize();
+    free_ws(c);
+    void* ws = nullptr;
+    if (cudaMalloc(&ws, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return MM_ERR_CUDA;
+    }
+    CK(cudaMemset(ws, 0, bytes));
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    c->idx = carve<int32_t>(p, npairs);
+    c->phys = carve<int32_t>(p, npairs);
+    c->pos = carve<int32_t>(p, npairs);
+    c->wgt = carve<float>(p, npairs);
+    c->chunk_hist = carve<int32_t>(p, chunks * c->P);
+    c->off = carve<int32_t>(p, c->P + 1);
+    c->tile_expert = carve<int32_t>(p, tiles);
+    c->tile_row0 = carve<int32_t>(p, tiles);
+    c->tile_rows = carve<int32_t>(p, tiles);
+    c->done1 = carve<int32_t>(p, tiles);
+    c->num_tiles = carve<int32_t>(p, 1);
+    c->xq = carve<uint8_t>(p, rows * H);
+    c->xs_t = carve<uint8_t>(p, rows * H / 32);
+    c->hq = carve<uint8_t>(p, rows * I);
+    c->hs_t = carve<uint8_t>(p, rows * I / 32);
+    c->y = carve<__nv_bfloat16>(p, rows * H);
+    c->ws = ws;
+    c->ws_bytes = bytes;
+    if (!make_map(&c->maps.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox) ||
+        !make_map(&c->maps.hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->hq, I, rows, I, mm::kBBox)) {
+        free_ws(c);
+        return MM_ERR_CUDA;
+    }
+    c->cap_tokens = max_tokens;
+    c->rows_cap = rows;
+    c->tiles_cap = tiles;
+    c->chunks_cap = chunks;
+    c->maps_ws = true;
+    return MM_OK;
+}
+
+mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const float* bias, void* out,
+                     int64_t T, mm_stream stream)
+{
+    if (!c || T < 0) return MM_ERR_INVALID_ARG;
+    if (!c->weights_set || !c->map_set) return MM_ERR_NOT_READY;
+    if (T == 0) return MM_OK;
+    if (!hidden || !logits || !out) return MM_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(logits, 4) || (bias && !aligned(bias, 4)))
+        return MM_ERR_INVALID_ARG;
+    if (T > c->cap_tokens) return MM_ERR_CAPACITY;
+    if (c->route == MM_ROUTE_SMALL && T > c->small_max) return MM_ERR_CAPACITY;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (mm::launch_quant_dispatch(c, hidden, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (mm::launch_gemm(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (mm::launch_combine(c, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    c->last_T = T;
+    c->last_stream = s;
+    return MM_OK;
+}
+
+mm_status mm_read_counts(mm_handle c, int layer, int64_t* out_host)
+{
+    if (!c || !out_host || layer < 0 || layer >= MM_MAX_LAYERS) return MM_ERR_INVALID_ARG;
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(out_host, c->counts + static_cast<int64_t>(layer) * c->E, sizeof(int64_t) * c->E,
+                  cudaMemcpyDeviceToHost));
+    int code = 0;
+    CK(cudaMemcpy(&code, c->status, sizeof(int), cudaMemcpyDeviceToHost));
+    return static_cast<mm_status>(code);
+}
+
+mm_status mm_reset_counts(mm_handle c, int layer)
+{
+    if (!c || layer < -1 || layer >= MM_MAX_LAYERS) return MM_ERR_INVALID_ARG;
+    CK(cudaDeviceSynchronize());
+    if (layer < 0) CK(cudaMemset(c->counts, 0, sizeof(int64_t) * MM_MAX_LAYERS * c->E));
+    else CK(cudaMemset(c->counts + static_cast<int64_t>(layer) * c->E, 0, sizeof(int64_t) * c->E));
+    return MM_OK;
+}
+
+mm_status mm_get_status(mm_handle c, int* device_code)
+{
+    if (!c || !device_code) return MM_ERR_INVALID_ARG;
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(device_code, c->status, sizeof(int), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(c->status, 0, sizeof(int)));
+    return MM_OK;
+}
+
+static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* rows_out)
+{
+    if (!c->ws || c->last_T == 0) {
+        *bytes = 0;
+        return MM_OK;
+    }
+    int32_t rows = 0;
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(&rows, c->off + c->P, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    *rows_out = rows;
+    const size_t pairs = static_cast<size_t>(c->last_T) * c->k;
+    switch (stage) {
+        case 0: case 1: case 2: case 3: *bytes = pairs * 4; break;
+        case 4: *bytes = (c->P + 1) * 4; break;
+        case 5: *bytes = static_cast<size_t>(rows) * c->H; break;
+        case 6: *bytes = static_cast<size_t>(rows) * c->H / 32; break;
+        case 7: *bytes = static_cast<size_t>(rows) * c->I; break;
+        case 8: *bytes = static_cast<size_t>(rows) * c->I / 32; break;
+        case 9: *bytes = static_cast<size_t>(rows) * c->H * 2; break;
+        default: return MM_ERR_INVALID_ARG;
+    }
+    return MM_OK;
+}
+
+mm_status mm_debug_size(mm_handle c, int stage, size_t* bytes)
+{
+    if (!c || !bytes) return MM_ERR_INVALID_ARG;
+    int32_t rows = 0;
+    return debug_geometry(c, stage, bytes, &rows);
+}
+
+mm_status mm_debug_dump(mm_handle c, int stage, void* dst, size_t bytes)
+{
+    if (!c || !dst) return MM_ERR_INVALID_ARG;
+    size_t full = 0;
+    int32_t rows = 0;
+    mm_status st = debug_geometry(c, stage, &full, &rows);
+    if (st != MM_OK) return st;
+    const size_t n = bytes < full ? bytes : full;
+    if (n == 0) return MM_OK;
+    const void* src = nullptr;
+    switch (stage) {
+        case 0: src = c->idx; break;
+        case 1: src = c->wgt; break;
+        case 2: src = c->phys; break;
+        case 3: src = c->pos; break;
+        case 4: src = c->off; break;
+        case 5: src = c->xq; break;
+        case 7: src = c->hq; break;
+        case 9: src = c->y; break;
+        default: break;
+    }
+    if (src) {
+        CK(cudaMemcpy(dst, src, n, cudaMemcpyDeviceToHost));
+        return MM_OK;
+    }
+    // scale stages: un-tile into row-major [rows][K/32]
+    const int K = stage == 6 ? c->H : c->I;
+    const uint8_t* tiled = stage == 6 ? c->xs_t : c->hs_t;
+    std::vector<uint8_t> t(full);
+    CK(cudaMemcpy(t.data(), tiled, full, cudaMemcpyDeviceToHost));
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    const int nb = K / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            const size_t at = static_cast<size_t>(r) * nb + b;
+            if (at < n) d[at] = t[mm::sf_tile_offset(r, b, K / 128)];
+        }
+    return MM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// mm_internal.h -- shared definitions of the fused MoE library: the handle,
+// tile geometry, the scale-factor tile layout and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/megamoe.h"
+
+namespace mm {
+
+// ---- tile geometry --------------------------------------------------------
+// Every physical expert's dispatched rows form a segment that starts at a
+// multiple of kTile rows, so one token tile never straddles two experts and
+// its activation scale factors fill whole scale tiles.
+constexpr int kTile = 128;       // token-tile rows, weight rows per MMA (M)
+constexpr int kKStep = 128;      // reduction elements per pipeline stage
+constexpr int kBBox = 16;        // token rows per TMA box of the B operand
+constexpr int kStages = 4;       // shared-memory pipeline depth
+constexpr int kChunkPairs = 1024;  // (token, slot) pairs per permute chunk
+
+// shared-memory stage: A0 | A1 | B | SF(A0, A1, B)
+constexpr int kATileBytes = kTile * kKStep;          // e2m1 unpacked to 1 byte/element in smem
+constexpr int kBTileBytes = kTile * kKStep;          // e4m3, up to 128 token rows
+constexpr int kSFBytes = 512;                        // 128 rows x 4 scale bytes
+constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes + 4 * kSFBytes;
+
+// Scale-factor tile layout, shared by weights and activations.  Rows are
+// grouped by 128 and K by 128 (4 scale bytes per row); each group is one
+// 512-byte tile in which row r, scale byte b sits at
+//     (r % 32) * 16 + ((r % 128) / 32) * 4 + b
+// -- the order in which tcgen05.cp 32x128b.warpx4 places scales in tensor
+// memory for the block-scaled MMA (one 32-bit column per 32-row quarter).
+__host__ __device__ inline int64_t sf_tile_offset(int64_t row, int kblock32, int kchunks)
+{
+    const int64_t rb = row / 128;
+    const int kc = kblock32 / 4;
+    return (rb * kchunks + kc) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + (kblock32 % 4);
+}
+
+struct GemmMaps {
+    CUtensorMap w1;   // e2m1 [P*2I rows][H]  (16 x 4-bit -> 16-byte smem units)
+    CUtensorMap w2;   // e2m1 [P*H rows][I]
+    CUtensorMap xq;   // e4m3 [rows][H]
+    CUtensorMap hq;   // e4m3 [rows][I]
+};
+
+struct GemmArgs {
+    const uint8_t* w1_sf;   // tiled [P][2I/128][H/128][512]
+    const uint8_t* w2_sf;   // tiled [P][H/128][I/128][512]
+    const uint8_t* xs_t;    // tiled [rows/128][H/128][512]
+    uint8_t* hq;            // [rows][I]
+    uint8_t* hs_t;          // tiled [rows/128][I/128][512]
+    __nv_bfloat16* y;       // [rows][H]
+    const int* tile_expert; // per token tile
+    const int* tile_row0;
+    const int* tile_rows;
+    const int* num_tiles;
+    int* done1;             // per token tile: GEMM1 units finished
+    int* status;
+    int H, I, P;
+    int phases;             // bit 0: GEMM1 units, bit 1: GEMM2 units
+};
+
+}  // namespace mm
+
+struct mm_ctx {
+    int dev = 0, sms = 0;
+    int E = 0, P = 0, k = 0, H = 0, I = 0;
+    int small_max = 512, large_min = 1024;
+    int route = MM_ROUTE_AUTO, layer = 0, recording = 0;
+    // weights (library-owned)
+    uint8_t *w1 = nullptr, *w1_sf = nullptr, *w2 = nullptr, *w2_sf = nullptr;
+    bool weights_set = false;
+    // EPLB map
+    int32_t *map = nullptr, *rc = nullptr;
+    int R = 1;
+    bool map_set = false;
+    // per-layer logical counts [MM_MAX_LAYERS][E]
+    int64_t* counts = nullptr;
+    // workspace
+    int64_t cap_tokens = 0, rows_cap = 0, tiles_cap = 0, chunks_cap = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t *idx = nullptr, *phys = nullptr, *pos = nullptr;
+    float* wgt = nullptr;
+    int32_t *chunk_hist = nullptr, *off = nullptr, *tile_expert = nullptr, *tile_row0 = nullptr,
+            *tile_rows = nullptr, *num_tiles = nullptr, *done1 = nullptr;
+    uint8_t *xq = nullptr, *xs_t = nullptr, *hq = nullptr, *hs_t = nullptr;
+    __nv_bfloat16* y = nullptr;
+    int* status = nullptr;
+    mm::GemmMaps maps{};
+    bool maps_weights = false, maps_ws = false;
+    // last forward (debug dumps)
+    int64_t last_T = 0;
+    cudaStream_t last_stream = nullptr;
+};
+
+namespace mm {
+
+// host-side launchers (return cudaGetLastError of the launch)
+cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias, int64_t T, cudaStream_t s);
+cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s);
+cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);
+cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s);
+cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s);
+cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s);
+cudaError_t gemm_prepare(int dev);
+
+}  // namespace mm

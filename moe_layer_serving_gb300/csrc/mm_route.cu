@@ -1,0 +1,432 @@
+// mm_route.cu -- the SIMT stages of the fused MoE forward on sm_103a:
+//   router (sigmoid top-k) + fused EPLB remap + per-expert load recording,
+//   the stable permute into expert-sorted 128-row segments,
+//   MXFP8 activation quantisation fused with the dispatch copy,
+//   the deterministic gather combine,
+//   and the re-layout of e8m0 scales into scale tiles (weights, at load time).
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "mm_device.cuh"
+#include "mm_internal.h"
+
+namespace mm {
+namespace {
+
+// ---------------------------------------------------------------------------
+// routing score: a fixed binary32 operation sequence (Cody-Waite reduction
+// with a two-part ln 2, degree-7 Taylor polynomial in Horner form, 2^n by the
+// exponent field), every step one IEEE-rounded add, mul or div and no fused
+// multiply-add, so the score -- and with it the selected experts -- is the
+// same on every machine that evaluates this sequence.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float exp_spec(float y)
+{
+    const float log2e = __uint_as_float(0x3FB8AA3Bu);
+    const float ln2_hi = __uint_as_float(0x3F317200u);
+    const float ln2_lo = __uint_as_float(0x35BFBE8Eu);
+    const float c2 = __uint_as_float(0x3F000000u);  // 1/2
+    const float c3 = __uint_as_float(0x3E2AAAABu);  // 1/6
+    const float c4 = __uint_as_float(0x3D2AAAABu);  // 1/24
+    const float c5 = __uint_as_float(0x3C088889u);  // 1/120
+    const float c6 = __uint_as_float(0x3AB60B61u);  // 1/720
+    const float c7 = __uint_as_float(0x39500D01u);  // 1/5040
+    y = fminf(fmaxf(y, -87.0f), 88.0f);
+    const float n = rintf(__fmul_rn(y, log2e));
+    float r = __fsub_rn(y, __fmul_rn(n, ln2_hi));
+    r = __fsub_rn(r, __fmul_rn(n, ln2_lo));
+    float p = c7;
+    p = __fadd_rn(__fmul_rn(p, r), c6);
+    p = __fadd_rn(__fmul_rn(p, r), c5);
+    p = __fadd_rn(__fmul_rn(p, r), c4);
+    p = __fadd_rn(__fmul_rn(p, r), c3);
+    p = __fadd_rn(__fmul_rn(p, r), c2);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    return __fmul_rn(p, exp2i(static_cast<int>(n)));
+}
+
+__device__ __forceinline__ float sigmoid_spec(float x)
+{
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_spec(-x)));
+}
+
+struct RouteArgs {
+    const float* logits;   // [T, E]
+    const float* bias;     // [E] or null
+    const int32_t* map;    // [E, R]
+    const int32_t* rc;     // [E]
+    int32_t* idx;          // [T, k]
+    float* w;              // [T, k]
+    int32_t* phys;         // [T, k]
+    int64_t* counts;       // [E] of the bound layer, or null when not recording
+    int64_t T;
+    int E, k, R;
+};
+
+constexpr int kRouteWarps = 8;
+
+// One warp per token.  Lane l holds experts l, l+32, ...; k rounds of a warp
+// arg-max over (key, -expert) select the experts in order, ties to the lower
+// expert index.  Counts go to shared memory first, then once per CTA to the
+// global per-layer table.
+template <int VPL>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a)
+{
+    __shared__ int hist[MM_MAX_EXPERTS];
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5);
+    if (t < a.T) {
+        float s[VPL], key[VPL];
+        uint32_t avail = 0;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            s[i] = 0.0f;
+            key[i] = 0.0f;
+            if (e < a.E) {
+                s[i] = sigmoid_spec(a.logits[t * a.E + e]);
+                key[i] = __fadd_rn(s[i], a.bias ? a.bias[e] : 0.0f);
+                avail |= 1u << i;
+            }
+        }
+        int sel_e[MM_MAX_TOPK];
+        float sel_s[MM_MAX_TOPK];
+#pragma unroll
+        for (int j = 0; j < MM_MAX_TOPK; ++j) {
+            if (j >= a.k) break;
+            float bk = -INFINITY, bs = 0.0f;
+            int be = 0x7FFFFFFF;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                if (((avail >> i) & 1u) && (be == 0x7FFFFFFF || key[i] > bk)) {
+                    bk = key[i];
+                    bs = s[i];
+                    be = lane + 32 * i;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
+                const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
+                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+                if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ok > bk || (ok == bk && oe < be))) {
+                    bk = ok;
+                    bs = os;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+            sel_e[j] = be;
+            sel_s[j] = bs;
+        }
+        if (lane == 0) {
+            float S = sel_s[0];
+            for (int j = 1; j < a.k; ++j) S = __fadd_rn(S, sel_s[j]);
+            for (int j = 0; j < a.k; ++j) {
+                const int e = sel_e[j];
+                const int slot = static_cast<int>((t + j) % a.rc[e]);
+                a.idx[t * a.k + j] = e;
+                a.w[t * a.k + j] = __fdiv_rn(sel_s[j], S);
+                a.phys[t * a.k + j] = a.map[static_cast<int64_t>(e) * a.R + slot];
+                if (a.counts) atomicAdd(&hist[e], 1);
+            }
+        }
+    }
+    if (a.counts) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < a.E; e += blockDim.x)
+            if (hist[e]) atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + e),
+                                   static_cast<unsigned long long>(hist[e]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// permute: chunk histograms -> per-expert scan (segments padded to 128 rows,
+// token-tile table) -> stable scatter (pairs keep (token, slot) order)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* phys, int64_t npairs, int P, int32_t* chunk_hist)
+{
+    __shared__ int hist[MM_MAX_EXPERTS];
+    for (int p = threadIdx.x; p < P; p += blockDim.x) hist[p] = 0;
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunkPairs;
+    for (int i = threadIdx.x; i < kChunkPairs; i += blockDim.x) {
+        const int64_t g = base + i;
+        if (g < npairs) atomicAdd(&hist[phys[g]], 1);
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) chunk_hist[static_cast<int64_t>(blockIdx.x) * P + p] = hist[p];
+}
+
+// inclusive block scan of one int per thread (blockDim.x = 512)
+__device__ int block_scan_incl(int v, int* warp_tot)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += o;
+    }
+    if (lane == 31) warp_tot[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int x = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, x, off);
+            if (lane >= off) x += o;
+        }
+        warp_tot[lane] = x;
+    }
+    __syncthreads();
+    const int add = w > 0 ? warp_tot[w - 1] : 0;
+    __syncthreads();
+    return v + add;
+}
+
+struct ScanArgs {
+    int32_t* chunk_hist;   // in: counts per chunk; out: exclusive base per chunk
+    int nchunks, P;
+    int32_t* off;          // [P+1] padded segment starts
+    int32_t* tile_expert;
+    int32_t* tile_row0;
+    int32_t* tile_rows;
+    int32_t* num_tiles;
+    int32_t* done1;
+};
+
+__global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
+{
+    __shared__ int warp_tot[32];
+    const int p = threadIdx.x;
+    int cnt = 0;
+    if (p < a.P) {
+        for (int c = 0; c < a.nchunks; ++c) {
+            int32_t* h = a.chunk_hist + static_cast<int64_t>(c) * a.P + p;
+            const int v = *h;
+            *h = cnt;
+            cnt += v;
+        }
+    }
+    const int padded = (cnt + kTile - 1) / kTile * kTile;
+    const int tiles = padded / kTile;
+    const int off_incl = block_scan_incl(padded, warp_tot);
+    const int tiles_incl = block_scan_incl(tiles, warp_tot);
+    if (p < a.P) {
+        const int off = off_incl - padded;
+        const int t0 = tiles_incl - tiles;
+        a.off[p] = off;
+        for (int t = 0; t < tiles; ++t) {
+            a.tile_expert[t0 + t] = p;
+            a.tile_row0[t0 + t] = off + t * kTile;
+            a.tile_rows[t0 + t] = min(kTile, cnt - t * kTile);
+            a.done1[t0 + t] = 0;
+        }
+        if (p == a.P - 1) {
+            a.off[a.P] = off_incl;
+            *a.num_tiles = tiles_incl;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(32) scatter_kernel(const int32_t* phys, int64_t npairs, int P,
+                                                     const int32_t* chunk_base, const int32_t* off, int32_t* pos)
+{
+    __shared__ int run[MM_MAX_EXPERTS];
+    const int lane = threadIdx.x;
+    for (int p = lane; p < P; p += 32) run[p] = 0;
+    __syncwarp();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunkPairs;
+    const int32_t* cb = chunk_base + static_cast<int64_t>(blockIdx.x) * P;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int it = 0; it < kChunkPairs / 32; ++it) {
+        const int64_t i = base + it * 32 + lane;
+        if (base + it * 32 >= npairs) break;
+        const bool valid = i < npairs;
+        const int p = valid ? phys[i] : -1;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
+        int before = 0;
+        if (valid) {
+            before = run[p];
+            pos[i] = off[p] + cb[p] + before + __popc(peers & lt);
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) run[p] = before + __popc(peers);
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 quantisation + dispatch: one thread per 32-element block of a token;
+// 4 x 128-bit loads, one e8m0 scale, 32 e4m3 codes written to each of the
+// token's k dispatch rows (2 x 128-bit stores each).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_dispatch_kernel(const __nv_bfloat16* __restrict__ x, int64_t T, int H,
+                                                            int k, const int32_t* __restrict__ pos,
+                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t)
+{
+    const int nb = H / 32;
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t t = g / nb;
+    const int b = static_cast<int>(g % nb);
+    if (t >= T) return;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + b * 32);
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(src + q);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[q * 8 + 2 * i] = __uint_as_float(w4[i] << 16);
+            v[q * 8 + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int X = mx_e4m3_exponent(amax);
+    const float inv = exp2i(-X);
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t wd = 0;
+        if (amax > 0.0f) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wd |= e4m3_code(v[4 * i + j], inv) << (8 * j);
+        }
+        packed[i] = wd;
+    }
+    const uint8_t sbyte = static_cast<uint8_t>(X + 127);
+    const int kchunks = H / 128;
+    for (int j = 0; j < k; ++j) {
+        const int64_t row = pos[t * k + j];
+        uint4* dst = reinterpret_cast<uint4*>(xq + row * H + b * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        xs_t[sf_tile_offset(row, b, kchunks)] = sbyte;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// combine: out[t] = bf16( sum_j w[t,j] * y[pos[t,j]] ), fp32, j in order; one
+// thread per 8 outputs (128-bit loads and stores), no atomics.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w,
+                                                     const int32_t* __restrict__ pos, int64_t T, int H, int k,
+                                                     __nv_bfloat16* __restrict__ out)
+{
+    const int nc = H / 8;
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t t = g / nc;
+    const int c = static_cast<int>(g % nc);
+    if (t >= T) return;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        const float wj = w[t * k + j];
+        const int64_t row = pos[t * k + j];
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(y + row * H) + c);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj, __uint_as_float(w4[i] << 16), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    reinterpret_cast<uint4*>(out + t * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void tile_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K)
+{
+    const int nb = K / 32;
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (g >= rows * nb) return;
+    const int64_t r = g / nb;
+    const int b = static_cast<int>(g % nb);
+    dst[sf_tile_offset(r, b, K / 128)] = src[g];
+}
+
+unsigned grid_for(int64_t threads, int block) { return static_cast<unsigned>((threads + block - 1) / block); }
+
+}  // namespace
+
+cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias, int64_t T, cudaStream_t s)
+{
+    RouteArgs a;
+    a.logits = logits;
+    a.bias = bias;
+    a.map = c->map;
+    a.rc = c->rc;
+    a.idx = c->idx;
+    a.w = c->wgt;
+    a.phys = c->phys;
+    a.counts = c->recording ? c->counts + static_cast<int64_t>(c->layer) * c->E : nullptr;
+    a.T = T;
+    a.E = c->E;
+    a.k = c->k;
+    a.R = c->R;
+    const unsigned grid = grid_for(T, kRouteWarps);
+    const int vpl = (c->E + 31) / 32;
+    if (vpl <= 4) route_kernel<4><<<grid, kRouteWarps * 32, 0, s>>>(a);
+    else if (vpl <= 8) route_kernel<8><<<grid, kRouteWarps * 32, 0, s>>>(a);
+    else route_kernel<16><<<grid, kRouteWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
+{
+    const int64_t npairs = T * c->k;
+    const int nchunks = static_cast<int>((npairs + kChunkPairs - 1) / kChunkPairs);
+    hist_kernel<<<nchunks, 256, 0, s>>>(c->phys, npairs, c->P, c->chunk_hist);
+    ScanArgs a;
+    a.chunk_hist = c->chunk_hist;
+    a.nchunks = nchunks;
+    a.P = c->P;
+    a.off = c->off;
+    a.tile_expert = c->tile_expert;
+    a.tile_row0 = c->tile_row0;
+    a.tile_rows = c->tile_rows;
+    a.num_tiles = c->num_tiles;
+    a.done1 = c->done1;
+    scan_kernel<<<1, 512, 0, s>>>(a);
+    scatter_kernel<<<nchunks, 32, 0, s>>>(c->phys, npairs, c->P, c->chunk_hist, c->off, c->pos);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s)
+{
+    const int64_t threads = T * (c->H / 32);
+    quant_dispatch_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hidden), T, c->H,
+                                                                 c->k, c->pos, c->xq, c->xs_t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s)
+{
+    const int64_t threads = T * (c->H / 8);
+    combine_kernel<<<grid_for(threads, 256), 256, 0, s>>>(c->y, c->wgt, c->pos, T, c->H, c->k,
+                                                          static_cast<__nv_bfloat16*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s)
+{
+    const int64_t threads = rows * (K / 32);
+    tile_scales_kernel<<<grid_for(threads, 256), 256, 0, s>>>(src, dst, rows, K);
+    return cudaGetLastError();
+}
+
+}  // namespace mm

@@ -1,0 +1,164 @@
+"""Shared plumbing of the GPU tests: run the library on seeded inputs and
+compare each stage with the CPU oracle (tests only)."""
+import numpy as np
+
+import oracle
+import synthetic
+from tests import helpers
+
+_WEIGHT_CACHE = {}
+
+
+def weights(cfg, physical=True):
+    key = (cfg.seed, cfg.E, cfg.H, cfg.I)
+    if key not in _WEIGHT_CACHE:
+        _WEIGHT_CACHE[key] = synthetic.make_all_weights(cfg, physical=False)
+    w = _WEIGHT_CACHE[key]
+    if physical and cfg.P != cfg.E:
+        p2l = synthetic.physical_to_logical(cfg)
+        return tuple(a[p2l] for a in w)
+    return w
+
+
+class Run:
+    """One handle with weights uploaded; forward() runs and collects dumps."""
+
+    def __init__(self, cfg, W=None, eplb=True, cap=None):
+        import torch
+        import moe_layer_serving_gb300 as mm
+        self.torch, self.mm, self.cfg = torch, mm, cfg
+        self.dev = torch.device("cuda:0")
+        self.op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I)
+        W = weights(cfg) if W is None else W
+        wt = [torch.from_numpy(np.ascontiguousarray(a)).to(self.dev) for a in W]
+        self.op.set_weights(*wt)
+        del wt
+        self.map = None
+        if cfg.P != cfg.E and eplb:
+            m, rc, _ = synthetic.make_eplb_map(cfg)
+            self.op.set_eplb_map(m, rc)
+            self.map = (m, rc)
+        self.op.reserve(cap or cfg.T)
+
+    def to_dev(self, hidden, logits, bias):
+        t = self.torch
+        x = t.from_numpy(np.ascontiguousarray(hidden).view(np.int16)).to(self.dev).view(t.bfloat16)
+        lg = t.from_numpy(np.ascontiguousarray(logits)).to(self.dev)
+        b = None if bias is None else t.from_numpy(np.ascontiguousarray(bias)).to(self.dev)
+        return x, lg, b
+
+    def forward(self, hidden, logits, bias, dumps=True):
+        t = self.torch
+        x, lg, b = self.to_dev(hidden, logits, bias)
+        out = t.empty_like(x)
+        self.op.forward(x, lg, b, out)
+        t.cuda.synchronize()
+        status = self.op.get_status()
+        res = {"out": out.view(t.int16).cpu().numpy().view(np.uint16), "status": status}
+        if dumps:
+            T, k = hidden.shape[0], self.cfg.k
+            for stage, (name, _) in self.mm.DUMP_STAGES.items():
+                a = self.op.debug_dump(stage)
+                if stage <= 3:
+                    a = a.reshape(T, k)
+                res[name] = a
+            rows = int(res["offsets"][-1])
+            H, I = self.cfg.H, self.cfg.I
+            res["xq"] = res["xq"].reshape(rows, H)
+            res["xs"] = res["xs"].reshape(rows, H // 32)
+            res["hq"] = res["hq"].reshape(rows, I)
+            res["hs"] = res["hs"].reshape(rows, I // 32)
+            res["y"] = res["y"].reshape(rows, H)
+        return res
+
+    def close(self):
+        self.op.close()
+
+
+def sample_tokens(T, n=24, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, T // 2, T - 1]
+    rest = rng.choice(T, size=min(T, n), replace=False)
+    return np.unique(np.clip(np.concatenate([fixed, rest]), 0, T - 1))
+
+
+def bf16_f64(bits):
+    return synthetic.f32_from_bf16_bits(bits).astype(np.float64)
+
+
+def assert_out_close(got_bits, ref_bits, what=""):
+    """The layer tolerance: relative L2 <= 1e-2 and every |err| <= 0.05 rms(ref)."""
+    got, ref = bf16_f64(got_bits), bf16_f64(ref_bits)
+    err = got - ref
+    rms = np.sqrt(np.mean(ref ** 2))
+    rel = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300)
+    assert rel <= 1e-2, f"{what} relative L2 {rel:.3e}"
+    assert np.abs(err).max() <= 0.05 * rms, f"{what} max |err| {np.abs(err).max():.3e} > 0.05 rms {rms:.3e}"
+    return rel
+
+
+def assert_mxfp8_close(q_gpu, s_gpu, q_ref, s_ref, min_equal=0.999):
+    """Requantised codes: nearly all identical, the rest one e4m3 step apart."""
+    a = helpers.deq_mxfp8(q_gpu, s_gpu)
+    b = helpers.deq_mxfp8(q_ref, s_ref)
+    X = np.repeat(np.maximum(s_gpu.astype(int), s_ref.astype(int)) - 127, 32, axis=-1)
+    step = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -3 + np.ldexp(1.0, X - 9)
+    assert np.all(np.abs(a - b) <= step * (1 + 1e-12)), "codes more than one e4m3 step apart"
+    same = np.mean((q_gpu == q_ref) & (np.repeat(s_gpu, 32, axis=-1) == np.repeat(s_ref, 32, axis=-1)))
+    assert same >= min_equal, f"only {same:.5f} of codes identical"
+    return same
+
+
+def check_against_oracle(cfg, res, hidden, logits, bias, W, map_rc, token_sel=None, check_hq=True):
+    """Every stage of one GPU forward against the oracle.
+
+    Routing, physical ids and the dispatch order are checked for all tokens;
+    the expert FFN and the output for token_sel (all tokens when None).
+    """
+    T, k, P = hidden.shape[0], cfg.k, cfg.P
+    m, rc = map_rc if map_rc is not None else (None, None)
+    idx, w = oracle.route(logits, bias, k)
+    assert np.array_equal(res["idx"], idx), "routing indices differ"
+    assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32)), "routing weights differ"
+    if m is None:
+        m_, rc_ = np.arange(cfg.E, dtype=np.int32)[:, None], np.ones(cfg.E, np.int32)
+    else:
+        m_, rc_ = m, rc
+    phys = oracle.eplb(idx, m_, rc_)
+    assert np.array_equal(res["phys"], phys), "physical experts differ"
+    off_o, order, pos_o = oracle.permute(phys, P)
+    cnt = np.diff(off_o)
+    padded = (cnt + 127) // 128 * 128
+    off_g = np.concatenate([[0], np.cumsum(padded)])
+    assert np.array_equal(res["offsets"], off_g), "segment offsets differ"
+    p_flat = phys.ravel()
+    rank_o = pos_o - off_o[p_flat]
+    rank_g = res["pos"].ravel() - off_g[p_flat]
+    assert np.array_equal(rank_g, rank_o), "dispatch order differs"
+
+    sel = np.arange(T) if token_sel is None else np.asarray(token_sel)
+    xq, xs = oracle.mxfp8_quant_bf16(hidden[sel])
+    for j in range(k):
+        rows = res["pos"][sel, j]
+        assert np.array_equal(res["xq"][rows], xq), "activation codes differ"
+        assert np.array_equal(res["xs"][rows], xs), "activation scales differ"
+
+    ref = oracle.forward(hidden[sel], logits[sel], bias, k, W, m, rc, token_ids=sel)
+    assert np.array_equal(ref["idx"], idx[sel])
+    rows = res["pos"][sel].ravel()                        # pair order (t, j)
+    if check_hq:
+        assert_mxfp8_close(res["hq"][rows], res["hs"][rows], ref["hq"], ref["hs"],
+                           min_equal=0.999 if rows.size * cfg.I >= 100000 else 0.995)
+    # teacher-forced GEMM2 + combine: the oracle consumes the GPU's hq/hs
+    ypair = np.empty((rows.size, cfg.H), np.float32)
+    psel = phys[sel].ravel()
+    for p in np.unique(psel):
+        at = np.nonzero(psel == p)[0]
+        ypair[at] = oracle.expert_down(res["hq"][rows[at]], res["hs"][rows[at]], W[2][p], W[3][p])
+    tf = oracle.combine(w[sel], ypair)
+    got, exp = bf16_f64(res["out"][sel]), bf16_f64(tf)
+    mag = np.abs(w[sel].astype(np.float64)[:, :, None] * ypair.reshape(len(sel), k, cfg.H)).sum(1)
+    bound = 2.0 ** -7 * mag + 2.0 ** -8 * np.abs(exp) + 1e-30
+    assert np.all(np.abs(got - exp) <= bound), "GEMM2/combine off beyond bf16 rounding"
+    rel = assert_out_close(res["out"][sel], ref["out"], "end to end")
+    return rel, ref

@@ -1,0 +1,201 @@
+"""Behaviour of the C ABI on the GPU: idle batches, capacity and route
+checks, per-layer recording slots, EPLB map validation, replica invariance,
+determinism and CUDA-graph capture."""
+import ctypes as C
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    return torch
+
+
+@pytest.fixture
+def small(torch):
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], P=12, recording=True)
+    run = gpu_util.Run(cfg, cap=64)
+    yield cfg, run
+    run.close()
+
+
+def test_idle_batch_is_a_noop(torch, small):
+    cfg, run = small
+    import moe_layer_serving_gb300 as mm
+    out = torch.full((4, cfg.H), 3.0, dtype=torch.bfloat16, device="cuda")
+    st = mm.lib().mm_forward(run.op.handle, None, None, None, None, 0, None)
+    assert st == mm.MM_OK
+    run.op.forward(out, torch.zeros(4, cfg.E, device="cuda"), None, out, num_tokens=0)
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
+    assert run.op.read_counts(0).sum() == 0
+
+
+def test_capacity_and_route_limits(torch, small):
+    cfg, run = small
+    import moe_layer_serving_gb300 as mm
+    x = torch.zeros(65, cfg.H, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(65, cfg.E, device="cuda")
+    L = mm.lib()
+    assert L.mm_forward(run.op.handle, x.data_ptr(), lg.data_ptr(), None, x.data_ptr(), 65, None) == \
+        mm.MM_ERR_CAPACITY
+    run.op.reserve(1024)
+    run.op.set_route(mm.ROUTE_SMALL)
+    x2 = torch.zeros(600, cfg.H, dtype=torch.bfloat16, device="cuda")
+    lg2 = torch.zeros(600, cfg.E, device="cuda")
+    out = torch.empty_like(x2)
+    assert L.mm_forward(run.op.handle, x2.data_ptr(), lg2.data_ptr(), None, out.data_ptr(), 600, None) == \
+        mm.MM_ERR_CAPACITY
+    run.op.set_route(mm.ROUTE_LARGE)
+    assert L.mm_forward(run.op.handle, x2.data_ptr(), lg2.data_ptr(), None, out.data_ptr(), 600, None) == mm.MM_OK
+    torch.cuda.synchronize()
+    assert L.mm_forward(run.op.handle, x2.data_ptr() + 2, lg2.data_ptr(), None, out.data_ptr(), 8, None) == \
+        mm.MM_ERR_INVALID_ARG
+    assert L.mm_set_route(run.op.handle, 7) == mm.MM_ERR_INVALID_ARG
+
+
+def test_forced_routes_agree(torch):
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    hidden, logits, bias = synthetic.make_activations(cfg, 200)
+    run = gpu_util.Run(cfg, cap=200)
+    outs = []
+    for r in (mm.ROUTE_SMALL, mm.ROUTE_LARGE, mm.ROUTE_AUTO):
+        run.op.set_route(r)
+        outs.append(run.forward(hidden, logits, bias, dumps=False)["out"])
+    run.close()
+    ref = oracle.forward(hidden, logits, bias, cfg.k, gpu_util.weights(cfg))["out"]
+    for o in outs:
+        gpu_util.assert_out_close(o, ref)
+
+
+def test_recording_slots_and_reset(torch, small):
+    cfg, run = small
+    hidden, logits, bias = synthetic.make_activations(cfg, 40)
+    idx, _ = oracle.route(logits, bias, cfg.k)
+    hist = np.bincount(idx.ravel(), minlength=cfg.E)
+    run.op.set_recording(False)
+    run.forward(hidden, logits, bias, dumps=False)
+    assert run.op.read_counts(0).sum() == 0
+    run.op.set_recording(True)
+    run.op.bind_layer(3)
+    run.forward(hidden, logits, bias, dumps=False)
+    run.forward(hidden, logits, bias, dumps=False)
+    run.op.bind_layer(7)
+    run.forward(hidden, logits, bias, dumps=False)
+    assert np.array_equal(run.op.read_counts(3), 2 * hist)
+    assert np.array_equal(run.op.read_counts(7), hist)
+    assert run.op.read_counts(0).sum() == 0
+    run.op.reset_counts(3)
+    assert run.op.read_counts(3).sum() == 0 and np.array_equal(run.op.read_counts(7), hist)
+    run.op.reset_counts(-1)
+    assert run.op.read_counts(7).sum() == 0
+
+
+def test_eplb_map_validation(torch):
+    import moe_layer_serving_gb300 as mm
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], P=12)
+    op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I)
+    W = [torch.from_numpy(a).cuda() for a in gpu_util.weights(cfg)]
+    op.set_weights(*W)
+    op.reserve(16)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    x = torch.from_numpy(hidden.view(np.int16)).cuda().view(torch.bfloat16)
+    lg = torch.from_numpy(logits).cuda()
+    out = torch.empty_like(x)
+    L = mm.lib()
+    # no map yet with P > E
+    assert L.mm_forward(op.handle, x.data_ptr(), lg.data_ptr(), None, out.data_ptr(), 16, None) == mm.MM_ERR_NOT_READY
+    m, rc, R = synthetic.make_eplb_map(cfg)
+    bad = m.copy()
+    bad[1, 0] = 0                              # physical 0 twice, physical 1 never
+    for mm_, rc_ in ((bad, rc), (m, np.where(rc == 2, 3, rc).astype(np.int32)), (m, np.zeros_like(rc))):
+        with pytest.raises(mm.MegaMoEError):
+            op.set_eplb_map(mm_, rc_)
+    op.set_eplb_map(m, rc)
+    assert L.mm_forward(op.handle, x.data_ptr(), lg.data_ptr(), None, out.data_ptr(), 16, None) == mm.MM_OK
+    torch.cuda.synchronize()
+    op.close()
+
+
+def test_replicas_give_identical_output(torch):
+    base = synthetic.CONFIGS[0]
+    hidden, logits, bias = synthetic.make_activations(base, 300)
+    a = gpu_util.Run(base, cap=300)
+    ra = a.forward(hidden, logits, bias)
+    a.close()
+    rep = dataclasses.replace(base, P=12)
+    b = gpu_util.Run(rep, cap=300)
+    rb = b.forward(hidden, logits, bias)
+    b.close()
+    assert np.any(rb["phys"] >= base.E)
+    assert np.array_equal(ra["out"], rb["out"])
+
+
+def test_deterministic_across_runs(torch):
+    cfg = synthetic.CONFIGS[0]
+    hidden, logits, bias = synthetic.make_activations(cfg, 257)
+    run = gpu_util.Run(cfg, cap=257)
+    o1 = run.forward(hidden, logits, bias, dumps=False)["out"]
+    o2 = run.forward(hidden, logits, bias, dumps=False)["out"]
+    run.close()
+    assert np.array_equal(o1, o2)
+
+
+def test_graph_capture_replay_matches_eager(torch):
+    cfg = synthetic.CONFIGS[0]
+    hidden, logits, bias = synthetic.make_activations(cfg, 96)
+    run = gpu_util.Run(cfg, cap=96)
+    x, lg, b = run.to_dev(hidden, logits, bias)
+    eager = torch.empty_like(x)
+    run.op.forward(x, lg, b, eager)
+    torch.cuda.synchronize()
+    out = torch.zeros_like(x)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run.op.forward(x, lg, b, out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    lg.copy_(torch.flip(lg, dims=[0]))
+    g.replay()
+    run.op.forward(x, lg, b, eager)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert run.op.get_status() == 0
+    run.close()
+
+
+def test_routing_bit_exact_wide_experts(torch):
+    # E = 512, k = 8, logits over a wide range with ties: the score sequence
+    # must select exactly the oracle's experts and reproduce its weights.
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], E=512, P=512, k=8, H=128, I=128)
+    T = 2048
+    rng = np.random.default_rng(11)
+    logits = (rng.standard_normal((T, cfg.E)) * rng.choice([0.01, 1, 10, 60], (T, 1))).astype(np.float32)
+    logits[::5, 1::2] = logits[::5, 0::2]
+    bias = (0.05 * rng.standard_normal(cfg.E)).astype(np.float32)
+    hidden = synthetic.bf16_bits_from_f32(rng.standard_normal((T, cfg.H)).astype(np.float32))
+    W = synthetic.make_all_weights(dataclasses.replace(cfg, E=cfg.E))
+    run = gpu_util.Run(cfg, W, cap=T)
+    res = run.forward(hidden, logits, bias)
+    run.close()
+    idx, w = oracle.route(logits, bias, cfg.k)
+    assert np.array_equal(res["idx"], idx)
+    assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32))
