@@ -1,0 +1,305 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused a8w4 MoE layer forward on GB300.
+
+One step = one layer forward (routing, EPLB remap/record, MXFP8 quant,
+dispatch, GEMM1+SwiGLU+requant, GEMM2, combine) over one batch of seeded
+synthetic tokens.  Default workload: the decode (small-input) layer, T=64
+tokens, H=7168, I=2048, 256 experts, top-6.  The expert weights (6 GB of
+MXFP4) are larger than L2, so consecutive steps stream them from HBM; no
+flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+Under torchrun each rank runs its own batch (independent replicas, no
+collective on the data path): weak scaling, value = tokens of all ranks /
+max-over-ranks time.  Prints one JSON line on rank 0.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+EXPERT_BYTES_PER_ELEM = 0.5 + 1.0 / 32      # packed e2m1 + one e8m0 byte per 32
+
+
+def expert_bytes(cfg) -> int:
+    return int((2 * cfg.I * cfg.H + cfg.H * cfg.I) * EXPERT_BYTES_PER_ELEM)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the oracle's timed sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
+    return ap.parse_args()
+
+
+def workload_config(cfg):
+    return {"workload": f"moe-layer-a8w4-T{cfg.T}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+            "P": cfg.P, "topk": cfg.k, "routing": "zipf" if cfg.zipf_s else "uniform",
+            "eplb_redundant": cfg.P - cfg.E, "l2": "weights 6 GB > L2, no flush",
+            "parallelism": "replicas"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons during the timed region."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens):
+    """Tokens/s of the CPU oracle on the first n_tokens of the batch."""
+    import oracle
+    sel = np.arange(min(n_tokens, hidden.shape[0]))
+    m, rc = pmap if pmap else (None, None)
+    t0 = time.perf_counter()
+    oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel)
+    dt = time.perf_counter() - t0
+    return sel.size / dt, dt, sel.size
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The oracle (plain C, fp64) timed on this machine's CPU cores."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    cfg = synthetic.CONFIGS[args.config]
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    W = synthetic.make_all_weights(cfg)
+    pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
+    n = min(args.cpu_sample, cfg.T)
+    for _ in range(max(0, args.warmup and 1)):
+        oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, 1)
+    times = []
+    for _ in range(args.steps):
+        _, dt, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n)
+        times.append(dt)
+    per_tok = statistics.median(times) / n
+    value = 1.0 / per_tok
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * cfg.T * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"first {n} of {cfg.T} tokens per step, all stages"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    import moe_layer_serving_gb300 as mm
+    from moe_layer_serving_gb300 import build as mbuild
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    mbuild.build()
+    dev = torch.device("cuda", local)
+    cfg = synthetic.CONFIGS[args.config]
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    W = synthetic.make_all_weights(cfg)
+    pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
+
+    op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I)
+    wt = [torch.from_numpy(a).to(dev) for a in W]
+    op.set_weights(*wt)
+    del wt
+    torch.cuda.empty_cache()
+    if pmap:
+        op.set_eplb_map(*pmap)
+    op.reserve(cfg.T)
+    op.set_recording(cfg.recording)
+    x = torch.from_numpy(hidden.view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(logits).to(dev)
+    b = torch.from_numpy(bias).to(dev)
+    out = torch.empty_like(x)
+    stream = torch.cuda.Stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-resident inputs: the kernel-level number ------------------
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            op.forward(x, lg, b, out, stream=stream)
+    stream.synchronize()
+    assert op.get_status() == 0
+    route, launches, _ = op.last_info()
+    phys = op.debug_dump(2)
+    touched = int(np.unique(phys).size)
+
+    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            op.set_profile_events(k_start[i], k_stop[i])
+            op.forward(x, lg, b, out, stream=stream)
+        ev1.record(stream)
+    stream.synchronize()
+    op.set_profile_events(None, None)
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(z) for a, z in zip(k_start, k_stop))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert op.get_status() == 0
+    value = cfg.T * world / (ms / 1e3)
+
+    # ---- end to end through the public call, host buffers ------------------
+    xh = torch.from_numpy(hidden.view(np.int16)).pin_memory()
+    lh = torch.from_numpy(logits).pin_memory()
+    oh = torch.empty((cfg.T, cfg.H), dtype=torch.int16).pin_memory()
+    xd = torch.empty_like(x)
+    ld = torch.empty_like(lg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                e0.record(stream)
+            xd.view(torch.int16).copy_(xh, non_blocking=True)
+            ld.copy_(lh, non_blocking=True)
+            op.forward(xd, ld, b, out, stream=stream)
+            oh.copy_(out.view(torch.int16), non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = cfg.T * world / (e2e_ms / 1e3)
+    h2d = hidden.nbytes + logits.nbytes
+    d2h = cfg.T * cfg.H * 2
+
+    # ---- roofline of the dominant kernel ------------------------------------
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+    if cfg.T <= 512:
+        alg = touched * expert_bytes(cfg)           # weight streaming: the touched experts' bytes
+        achieved = alg / (kern_ms / 1e3) / 1e9
+        peak = peaks.get("hbm_gbs", 6800.0)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "gemm_kernel", "algorithmic_bytes": alg,
+                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
+    else:
+        flops = 6.0 * cfg.T * cfg.k * cfg.H * cfg.I
+        achieved = flops / (kern_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops", 1900.0) * 2.0   # fp8-class MMA: 2x the bf16 rate
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "gemm_kernel", "algorithmic_flops": flops,
+                "peak_source": "measured bf16 x 2" if "bf16_tflops" in peaks else "fallback x 2"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3xe2m1->f32", "data": "synthetic (seeded, random-init weights)",
+        "config": workload_config(cfg), "clocks": clk, "gpu_launches": launches * args.steps,
+        "route": "small" if route == 1 else "large", "kernel_ms": kern_ms, "touched_experts": touched,
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": roof,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_sample)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                                "sample": f"first {n} of {cfg.T} tokens, all stages, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    op.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -173,8 +173,19 @@ MM_API mm_status mm_get_status(mm_handle h, int *device_code);
  * dst_host; MM_ERR_INVALID_ARG for an unknown stage. */
 MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t bytes);
 
+/* Stage 10 of mm_debug_dump: int32 [3] = {route taken by the last forward
+ * (1 small, 2 large), number of kernels it launched, site of the last
+ * device-side timeout (0 none; see WaitSite in the sources)}. */
+
 /* Size in bytes of a debug stage for the last forward (0 before any). */
 MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);
+
+/* Profiling hook: when start/stop are non-NULL cudaEvent_t handles, every
+ * later mm_forward records `start` on its stream right before the launch of
+ * its dominant kernel (the grouped GEMM, or the fused small-input kernel) and
+ * `stop` right after it; NULL, NULL turns this off.  The events stay owned by
+ * the caller and may be replaced between forwards. */
+MM_API mm_status mm_set_profile_events(mm_handle h, void *start, void *stop);
 
 /* Short text for a status code (static storage). */
 MM_API const char *mm_status_string(mm_status s);

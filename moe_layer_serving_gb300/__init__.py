@@ -27,7 +27,7 @@ ROUTE_AUTO, ROUTE_SMALL, ROUTE_LARGE = 0, 1, 2
 # debug stage -> (name, numpy dtype, per-row width: None = flat)
 DUMP_STAGES = {0: ("idx", np.int32), 1: ("weights", np.float32), 2: ("phys", np.int32), 3: ("pos", np.int32),
                4: ("offsets", np.int32), 5: ("xq", np.uint8), 6: ("xs", np.uint8), 7: ("hq", np.uint8),
-               8: ("hs", np.uint8), 9: ("y", np.uint16)}
+               8: ("hs", np.uint8), 9: ("y", np.uint16), 10: ("info", np.int32)}
 
 _p, _i32, _i64, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
 _SIGS = {
@@ -45,6 +45,7 @@ _SIGS = {
     "mm_get_status": [_p, C.POINTER(_i32)],
     "mm_debug_dump": [_p, _i32, _p, _sz],
     "mm_debug_size": [_p, _i32, C.POINTER(_sz)],
+    "mm_set_profile_events": [_p, _p, _p],
 }
 _lib = None
 
@@ -175,6 +176,18 @@ class MegaMoE:
         code = C.c_int(0)
         _check(lib().mm_get_status(self._h, C.byref(code)), "mm_get_status")
         return code.value
+
+    def set_profile_events(self, start=None, stop=None) -> None:
+        """torch.cuda.Event pair (or None, None) recorded around the dominant kernel."""
+        s = None if start is None else start.cuda_event
+        e = None if stop is None else stop.cuda_event
+        _check(lib().mm_set_profile_events(self._h, s, e), "mm_set_profile_events")
+
+    def last_info(self) -> tuple[int, int, int]:
+        """(route taken: 1 small / 2 large, kernels launched, site of the last
+        device-side timeout or 0) of the last forward."""
+        a = self.debug_dump(10)
+        return int(a[0]), int(a[1]), int(a[2])
 
     def debug_dump(self, stage: int) -> np.ndarray:
         n = C.c_size_t(0)

@@ -140,7 +140,8 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
     if (mm::gemm_prepare(dev) != cudaSuccess ||
         cudaMalloc(&c->counts, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
         cudaMemset(c->counts, 0, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
-        cudaMalloc(&c->status, sizeof(int)) != cudaSuccess || cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaMalloc(&c->status, 2 * sizeof(int)) != cudaSuccess ||
+        cudaMemset(c->status, 0, 2 * sizeof(int)) != cudaSuccess) {
         cudaGetLastError();
         mm_destroy(c);
         return MM_ERR_CUDA;
@@ -340,10 +341,23 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_quant_dispatch(c, hidden, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (c->prof_start && cudaEventRecord(c->prof_start, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_gemm(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (c->prof_stop && cudaEventRecord(c->prof_stop, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_combine(c, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    const bool small = c->route == MM_ROUTE_SMALL || (c->route == MM_ROUTE_AUTO && T <= c->small_max);
+    c->last_route = small ? 1 : 2;
+    c->last_launches = 7;
     c->last_T = T;
     c->last_stream = s;
+    return MM_OK;
+}
+
+mm_status mm_set_profile_events(mm_handle c, void* start, void* stop)
+{
+    if (!c || (start == nullptr) != (stop == nullptr)) return MM_ERR_INVALID_ARG;
+    c->prof_start = static_cast<cudaEvent_t>(start);
+    c->prof_stop = static_cast<cudaEvent_t>(stop);
     return MM_OK;
 }
 
@@ -371,8 +385,11 @@ mm_status mm_get_status(mm_handle c, int* device_code)
 {
     if (!c || !device_code) return MM_ERR_INVALID_ARG;
     CK(cudaDeviceSynchronize());
-    CK(cudaMemcpy(device_code, c->status, sizeof(int), cudaMemcpyDeviceToHost));
-    CK(cudaMemset(c->status, 0, sizeof(int)));
+    int st[2] = {0, 0};
+    CK(cudaMemcpy(st, c->status, sizeof(st), cudaMemcpyDeviceToHost));
+    *device_code = st[0];
+    c->last_site = st[1];
+    CK(cudaMemset(c->status, 0, sizeof(st)));
     return MM_OK;
 }
 
@@ -395,6 +412,7 @@ static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* 
         case 7: *bytes = static_cast<size_t>(rows) * c->I; break;
         case 8: *bytes = static_cast<size_t>(rows) * c->I / 32; break;
         case 9: *bytes = static_cast<size_t>(rows) * c->H * 2; break;
+        case 10: *bytes = 3 * sizeof(int32_t); break;
         default: return MM_ERR_INVALID_ARG;
     }
     return MM_OK;
@@ -416,6 +434,13 @@ mm_status mm_debug_dump(mm_handle c, int stage, void* dst, size_t bytes)
     if (st != MM_OK) return st;
     const size_t n = bytes < full ? bytes : full;
     if (n == 0) return MM_OK;
+    if (stage == 10) {
+        int32_t site = 0;
+        CK(cudaMemcpy(&site, c->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost));
+        const int32_t info[3] = {c->last_route, c->last_launches, site ? site : c->last_site};
+        memcpy(dst, info, n);
+        return MM_OK;
+    }
     const void* src = nullptr;
     switch (stage) {
         case 0: src = c->idx; break;

@@ -27,9 +27,10 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
-__device__ __forceinline__ void latch_error(int* status, int code)
+// status[0] = first error code, status[1] = the site that raised it
+__device__ __forceinline__ void latch_error(int* status, int code, int site = 0)
 {
-    atomicCAS(status, 0, code);
+    if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, site);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -76,14 +77,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 
 // Wait for the phase with the given parity to complete; false on timeout
 // (then MM_ERR_TIMEOUT is latched and *abort set so the caller unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort,
+                                          int site)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
-            latch_error(status, MM_ERR_TIMEOUT);
+            latch_error(status, MM_ERR_TIMEOUT, site);
             *abort = 1;
             return false;
         }

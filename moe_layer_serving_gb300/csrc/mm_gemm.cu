@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         while (ld_acquire(&g.done1[un.tile]) < need) {
                             if (*abort_flag) break;
                             if (globaltimer() - t0 > kWaitLimitNs) {
-                                latch_error(g.status, MM_ERR_TIMEOUT);
+                                latch_error(g.status, MM_ERR_TIMEOUT, kSiteProducerDone1);
                                 *abort_flag = 1;
                                 break;
                             }
@@ -164,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (*abort_flag) break;
                 }
                 const int nbox = un.n / kBBox;
-                const uint32_t bytes = un.na * kATileBytes + nbox * kBBox * kKStep + (un.na + 1) * kSFBytes;
+                const uint32_t bytes = un.na * kATileTxBytes + nbox * kBBox * kKStep + (un.na + 1) * kSFBytes;
                 for (int ks = 0; ks < un.ksteps; ++ks) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, g.status, abort_flag)) break;
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, g.status, abort_flag, kSiteProducerEmpty)) break;
                     uint8_t* st = smem + stage * kStageBytes;
                     uint8_t* sf = st + 2 * kATileBytes + kBTileBytes;
                     mbar_arrive_expect_tx(&full[stage], bytes);
@@ -205,10 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             Unit un;
             for (int u = blockIdx.x; decode_unit(g, ntiles, u, un) && !*abort_flag; u += gridDim.x) {
-                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, g.status, abort_flag)) break;
+                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, g.status, abort_flag, kSiteMmaTmemEmpty)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < un.ksteps; ++ks) {
-                    if (!mbar_wait(&full[stage], phase, g.status, abort_flag)) break;
+                    if (!mbar_wait(&full[stage], phase, g.status, abort_flag, kSiteMmaFull)) break;
                     tc_fence_after();
                     uint8_t* st = smem + stage * kStageBytes;
                     uint8_t* sf = st + 2 * kATileBytes + kBTileBytes;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_phase = 0;
         Unit un;
         for (int u = blockIdx.x; decode_unit(g, ntiles, u, un) && !*abort_flag; u += gridDim.x) {
-            if (!mbar_wait(tmem_full, acc_phase, g.status, abort_flag)) break;
+            if (!mbar_wait(tmem_full, acc_phase, g.status, abort_flag, kSiteEpiTmemFull)) break;
             tc_fence_after();
             if (un.phase == 1) {
                 const int col = un.blk * kTile + 32 * q + lane;   // column of h (I axis)

@@ -23,6 +23,7 @@ constexpr int kChunkPairs = 1024;  // (token, slot) pairs per permute chunk
 
 // shared-memory stage: A0 | A1 | B | SF(A0, A1, B)
 constexpr int kATileBytes = kTile * kKStep;          // e2m1 unpacked to 1 byte/element in smem
+constexpr int kATileTxBytes = kTile * kKStep / 2;    // what the TMA counts: the packed global bytes
 constexpr int kBTileBytes = kTile * kKStep;          // e4m3, up to 128 token rows
 constexpr int kSFBytes = 512;                        // 128 rows x 4 scale bytes
 constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes + 4 * kSFBytes;
@@ -93,12 +94,25 @@ struct mm_ctx {
     int* status = nullptr;
     mm::GemmMaps maps{};
     bool maps_weights = false, maps_ws = false;
+    // profiling events around the dominant kernel (caller-owned)
+    cudaEvent_t prof_start = nullptr, prof_stop = nullptr;
     // last forward (debug dumps)
+    int last_route = 0, last_launches = 0, last_site = 0;
     int64_t last_T = 0;
     cudaStream_t last_stream = nullptr;
 };
 
 namespace mm {
+
+// sites of a device-side timeout (status[1])
+enum WaitSite {
+    kSiteProducerEmpty = 1,
+    kSiteMmaFull = 2,
+    kSiteMmaTmemEmpty = 3,
+    kSiteEpiTmemFull = 4,
+    kSiteProducerDone1 = 5,
+    kSiteGridBarrier = 6,
+};
 
 // host-side launchers (return cudaGetLastError of the launch)
 cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias, int64_t T, cudaStream_t s);
