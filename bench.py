@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the oracle's timed sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E = P (a smaller case of the same kernels, for profiler captures)")
     return ap.parse_args()
 
 
@@ -169,6 +171,9 @@ def main():
     mbuild.build()
     dev = torch.device("cuda", local)
     cfg = synthetic.CONFIGS[args.config]
+    if args.experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, E=args.experts, P=args.experts, zipf_s=0.0)
     hidden, logits, bias = synthetic.make_activations(cfg)
     W = synthetic.make_all_weights(cfg)
     pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
@@ -203,8 +208,7 @@ def main():
     phys = op.debug_dump(2)
     touched = int(np.unique(phys).size)
 
-    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    op.profile_begin(args.steps)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     barrier()
@@ -214,16 +218,15 @@ def main():
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for i in range(args.steps):
-            op.set_profile_events(k_start[i], k_stop[i])
             op.forward(x, lg, b, out, stream=stream)
         ev1.record(stream)
     stream.synchronize()
-    op.set_profile_events(None, None)
+    kern = op.profile_end()
     clk = clocks.stop()
     torch.cuda.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
-    kern_ms = statistics.mean(a.elapsed_time(z) for a, z in zip(k_start, k_stop))
+    kern_ms = float(np.mean(kern))
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms], device=dev)

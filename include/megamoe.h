@@ -180,12 +180,15 @@ MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t by
 /* Size in bytes of a debug stage for the last forward (0 before any). */
 MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);
 
-/* Profiling hook: when start/stop are non-NULL cudaEvent_t handles, every
- * later mm_forward records `start` on its stream right before the launch of
- * its dominant kernel (the grouped GEMM, or the fused small-input kernel) and
- * `stop` right after it; NULL, NULL turns this off.  The events stay owned by
- * the caller and may be replaced between forwards. */
-MM_API mm_status mm_set_profile_events(mm_handle h, void *start, void *stop);
+/* Per-launch timing of the dominant kernel (the grouped GEMM, or the fused
+ * small-input kernel).  mm_profile_begin creates max_launches pairs of CUDA
+ * events (allocation: call it outside stream capture); each later mm_forward
+ * records one pair on its stream right around that kernel, until
+ * max_launches forwards have been recorded.  mm_profile_end synchronises,
+ * writes up to max_out durations in milliseconds to ms_out (host), stores
+ * how many in *n_out, and stops recording. */
+MM_API mm_status mm_profile_begin(mm_handle h, int max_launches);
+MM_API mm_status mm_profile_end(mm_handle h, float *ms_out, int max_out, int *n_out);
 
 /* Short text for a status code (static storage). */
 MM_API const char *mm_status_string(mm_status s);

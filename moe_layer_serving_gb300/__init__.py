@@ -45,7 +45,8 @@ _SIGS = {
     "mm_get_status": [_p, C.POINTER(_i32)],
     "mm_debug_dump": [_p, _i32, _p, _sz],
     "mm_debug_size": [_p, _i32, C.POINTER(_sz)],
-    "mm_set_profile_events": [_p, _p, _p],
+    "mm_profile_begin": [_p, _i32],
+    "mm_profile_end": [_p, _p, _i32, C.POINTER(_i32)],
 }
 _lib = None
 
@@ -177,11 +178,16 @@ class MegaMoE:
         _check(lib().mm_get_status(self._h, C.byref(code)), "mm_get_status")
         return code.value
 
-    def set_profile_events(self, start=None, stop=None) -> None:
-        """torch.cuda.Event pair (or None, None) recorded around the dominant kernel."""
-        s = None if start is None else start.cuda_event
-        e = None if stop is None else stop.cuda_event
-        _check(lib().mm_set_profile_events(self._h, s, e), "mm_set_profile_events")
+    def profile_begin(self, max_launches: int) -> None:
+        """Record the dominant kernel's duration for the next max_launches forwards."""
+        _check(lib().mm_profile_begin(self._h, max_launches), "mm_profile_begin")
+
+    def profile_end(self) -> np.ndarray:
+        """Durations (ms) recorded since profile_begin."""
+        buf = np.zeros(100000, np.float32)
+        n = C.c_int(0)
+        _check(lib().mm_profile_end(self._h, buf.ctypes.data, buf.size, C.byref(n)), "mm_profile_end")
+        return buf[: n.value].copy()
 
     def last_info(self) -> tuple[int, int, int]:
         """(route taken: 1 small / 2 large, kernels launched, site of the last

@@ -94,6 +94,14 @@ void free_ws(mm_ctx* c)
     c->maps_ws = false;
 }
 
+void profile_free(mm_ctx* c)
+{
+    for (cudaEvent_t e : c->prof_events)
+        if (e) cudaEventDestroy(e);
+    c->prof_events.clear();
+    c->prof_used = 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,6 +173,7 @@ mm_status mm_destroy(mm_handle c)
     cudaDeviceSynchronize();
     cudaGetLastError();
     free_ws(c);
+    profile_free(c);
     void* ptrs[] = {c->w1, c->w1_sf, c->w2, c->w2_sf, c->map, c->rc, c->counts, c->status};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -341,9 +350,11 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_quant_dispatch(c, hidden, T, s) != cudaSuccess) return MM_ERR_CUDA;
-    if (c->prof_start && cudaEventRecord(c->prof_start, s) != cudaSuccess) return MM_ERR_CUDA;
+    const bool prof = c->prof_used < static_cast<int>(c->prof_events.size()) / 2;
+    if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used], s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_gemm(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
-    if (c->prof_stop && cudaEventRecord(c->prof_stop, s) != cudaSuccess) return MM_ERR_CUDA;
+    if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used + 1], s) != cudaSuccess) return MM_ERR_CUDA;
+    if (prof) ++c->prof_used;
     if (mm::launch_combine(c, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
     const bool small = c->route == MM_ROUTE_SMALL || (c->route == MM_ROUTE_AUTO && T <= c->small_max);
     c->last_route = small ? 1 : 2;
@@ -353,11 +364,31 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     return MM_OK;
 }
 
-mm_status mm_set_profile_events(mm_handle c, void* start, void* stop)
+mm_status mm_profile_begin(mm_handle c, int max_launches)
 {
-    if (!c || (start == nullptr) != (stop == nullptr)) return MM_ERR_INVALID_ARG;
-    c->prof_start = static_cast<cudaEvent_t>(start);
-    c->prof_stop = static_cast<cudaEvent_t>(stop);
+    if (!c || max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;
+    profile_free(c);
+    c->prof_events.resize(2 * static_cast<size_t>(max_launches));
+    for (auto& e : c->prof_events) {
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            cudaGetLastError();
+            e = nullptr;
+            profile_free(c);
+            return MM_ERR_CUDA;
+        }
+    }
+    return MM_OK;
+}
+
+mm_status mm_profile_end(mm_handle c, float* ms_out, int max_out, int* n_out)
+{
+    if (!c || !n_out || (max_out > 0 && !ms_out)) return MM_ERR_INVALID_ARG;
+    *n_out = 0;
+    CK(cudaDeviceSynchronize());
+    const int n = c->prof_used < max_out ? c->prof_used : max_out;
+    for (int i = 0; i < n; ++i) CK(cudaEventElapsedTime(&ms_out[i], c->prof_events[2 * i], c->prof_events[2 * i + 1]));
+    *n_out = n;
+    profile_free(c);
     return MM_OK;
 }
 

@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/megamoe.h"
 
 namespace mm {
@@ -94,8 +96,9 @@ struct mm_ctx {
     int* status = nullptr;
     mm::GemmMaps maps{};
     bool maps_weights = false, maps_ws = false;
-    // profiling events around the dominant kernel (caller-owned)
-    cudaEvent_t prof_start = nullptr, prof_stop = nullptr;
+    // per-launch timing of the dominant kernel: event pairs, pairs recorded so far
+    std::vector<cudaEvent_t> prof_events;
+    int prof_used = 0;
     // last forward (debug dumps)
     int last_route = 0, last_launches = 0, last_site = 0;
     int64_t last_T = 0;
