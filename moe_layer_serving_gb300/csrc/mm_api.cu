@@ -143,9 +143,10 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
     c->k = k;
     c->H = H;
     c->I = I;
-    c->small_max = env_int("MM_SMALL_M_MAX", 512);
+    c->small_max = env_int("MM_SMALL_M_MAX", mm::kSmallMaxTokens);
+    if (c->small_max > mm::kSmallMaxTokens) c->small_max = mm::kSmallMaxTokens;
     c->large_min = env_int("MM_LARGE_M_MIN", 1024);
-    if (mm::gemm_prepare(dev) != cudaSuccess ||
+    if (mm::gemm_prepare(dev) != cudaSuccess || mm::small_prepare() != cudaSuccess ||
         cudaMalloc(&c->counts, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
         cudaMemset(c->counts, 0, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
         cudaMalloc(&c->status, 2 * sizeof(int)) != cudaSuccess ||
@@ -294,6 +295,7 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     add(rows * I);
     add(rows * I / 32);
     add(rows * H * 2);
+    add(64);                                  // grid barrier
     bytes += 8 * 256;
     cudaDeviceSynchronize();
     free_ws(c);
@@ -320,6 +322,7 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->hq = carve<uint8_t>(p, rows * I);
     c->hs_t = carve<uint8_t>(p, rows * I / 32);
     c->y = carve<__nv_bfloat16>(p, rows * H);
+    c->grid_bar = carve<unsigned>(p, 16);
     c->ws = ws;
     c->ws_bytes = bytes;
     if (!make_map(&c->maps.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox) ||
@@ -347,18 +350,25 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     if (T > c->cap_tokens) return MM_ERR_CAPACITY;
     if (c->route == MM_ROUTE_SMALL && T > c->small_max) return MM_ERR_CAPACITY;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
-    if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
-    if (mm::launch_quant_dispatch(c, hidden, T, s) != cudaSuccess) return MM_ERR_CUDA;
-    const bool prof = c->prof_used < static_cast<int>(c->prof_events.size()) / 2;
-    if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used], s) != cudaSuccess) return MM_ERR_CUDA;
-    if (mm::launch_gemm(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
-    if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used + 1], s) != cudaSuccess) return MM_ERR_CUDA;
-    if (prof) ++c->prof_used;
-    if (mm::launch_combine(c, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
     const bool small = c->route == MM_ROUTE_SMALL || (c->route == MM_ROUTE_AUTO && T <= c->small_max);
+    const bool prof = c->prof_used < static_cast<int>(c->prof_events.size()) / 2;
+    if (small) {
+        // one cooperative launch: every stage of the layer
+        if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used], s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_small(c, hidden, logits, bias, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used + 1], s) != cudaSuccess) return MM_ERR_CUDA;
+    } else {
+        if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_quant_dispatch(c, hidden, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used], s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_gemm(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (prof && cudaEventRecord(c->prof_events[2 * c->prof_used + 1], s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_combine(c, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
+    }
+    if (prof) ++c->prof_used;
     c->last_route = small ? 1 : 2;
-    c->last_launches = 7;
+    c->last_launches = small ? 1 : 7;
     c->last_T = T;
     c->last_stream = s;
     return MM_OK;
@@ -421,6 +431,7 @@ mm_status mm_get_status(mm_handle c, int* device_code)
     *device_code = st[0];
     c->last_site = st[1];
     CK(cudaMemset(c->status, 0, sizeof(st)));
+    if (st[0] != 0 && c->grid_bar) CK(cudaMemset(c->grid_bar, 0, 16 * sizeof(unsigned)));
     return MM_OK;
 }
 

@@ -22,6 +22,7 @@ constexpr int kKStep = 128;      // reduction elements per pipeline stage
 constexpr int kBBox = 16;        // token rows per TMA box of the B operand
 constexpr int kStages = 4;       // shared-memory pipeline depth
 constexpr int kChunkPairs = 1024;  // (token, slot) pairs per permute chunk
+constexpr int kSmallMaxTokens = 512;  // largest batch the fused small-input kernel takes
 
 // shared-memory stage: A0 | A1 | B | SF(A0, A1, B)
 constexpr int kATileBytes = kTile * kKStep;          // e2m1 unpacked to 1 byte/element in smem
@@ -94,6 +95,7 @@ struct mm_ctx {
     uint8_t *xq = nullptr, *xs_t = nullptr, *hq = nullptr, *hs_t = nullptr;
     __nv_bfloat16* y = nullptr;
     int* status = nullptr;
+    unsigned* grid_bar = nullptr;   // fused kernel's grid barrier {count, generation}
     mm::GemmMaps maps{};
     bool maps_weights = false, maps_ws = false;
     // per-launch timing of the dominant kernel: event pairs, pairs recorded so far
@@ -125,5 +127,9 @@ cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s);
 cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s);
 cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s);
 cudaError_t gemm_prepare(int dev);
+cudaError_t small_prepare();
+cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logits, const float* bias, void* out,
+                         int64_t T, cudaStream_t s);
+void fill_gemm_args(const mm_ctx* c, GemmArgs* g);
 
 }  // namespace mm

@@ -10,133 +10,22 @@
 
 #include "mm_device.cuh"
 #include "mm_internal.h"
+#include "mm_stages.cuh"
 
 namespace mm {
 namespace {
 
-// ---------------------------------------------------------------------------
-// routing score: a fixed binary32 operation sequence (Cody-Waite reduction
-// with a two-part ln 2, degree-7 Taylor polynomial in Horner form, 2^n by the
-// exponent field), every step one IEEE-rounded add, mul or div and no fused
-// multiply-add, so the score -- and with it the selected experts -- is the
-// same on every machine that evaluates this sequence.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float exp_spec(float y)
-{
-    const float log2e = __uint_as_float(0x3FB8AA3Bu);
-    const float ln2_hi = __uint_as_float(0x3F317200u);
-    const float ln2_lo = __uint_as_float(0x35BFBE8Eu);
-    const float c2 = __uint_as_float(0x3F000000u);  // 1/2
-    const float c3 = __uint_as_float(0x3E2AAAABu);  // 1/6
-    const float c4 = __uint_as_float(0x3D2AAAABu);  // 1/24
-    const float c5 = __uint_as_float(0x3C088889u);  // 1/120
-    const float c6 = __uint_as_float(0x3AB60B61u);  // 1/720
-    const float c7 = __uint_as_float(0x39500D01u);  // 1/5040
-    y = fminf(fmaxf(y, -87.0f), 88.0f);
-    const float n = rintf(__fmul_rn(y, log2e));
-    float r = __fsub_rn(y, __fmul_rn(n, ln2_hi));
-    r = __fsub_rn(r, __fmul_rn(n, ln2_lo));
-    float p = c7;
-    p = __fadd_rn(__fmul_rn(p, r), c6);
-    p = __fadd_rn(__fmul_rn(p, r), c5);
-    p = __fadd_rn(__fmul_rn(p, r), c4);
-    p = __fadd_rn(__fmul_rn(p, r), c3);
-    p = __fadd_rn(__fmul_rn(p, r), c2);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    return __fmul_rn(p, exp2i(static_cast<int>(n)));
-}
-
-__device__ __forceinline__ float sigmoid_spec(float x)
-{
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_spec(-x)));
-}
-
-struct RouteArgs {
-    const float* logits;   // [T, E]
-    const float* bias;     // [E] or null
-    const int32_t* map;    // [E, R]
-    const int32_t* rc;     // [E]
-    int32_t* idx;          // [T, k]
-    float* w;              // [T, k]
-    int32_t* phys;         // [T, k]
-    int64_t* counts;       // [E] of the bound layer, or null when not recording
-    int64_t T;
-    int E, k, R;
-};
-
 constexpr int kRouteWarps = 8;
 
-// One warp per token.  Lane l holds experts l, l+32, ...; k rounds of a warp
-// arg-max over (key, -expert) select the experts in order, ties to the lower
-// expert index.  Counts go to shared memory first, then once per CTA to the
-// global per-layer table.
-template <int VPL>
+// One warp per token; selections counted in shared memory, then once per CTA
+// into the bound layer's global count table.
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a)
 {
     __shared__ int hist[MM_MAX_EXPERTS];
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
-
-    const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5);
-    if (t < a.T) {
-        float s[VPL], key[VPL];
-        uint32_t avail = 0;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            s[i] = 0.0f;
-            key[i] = 0.0f;
-            if (e < a.E) {
-                s[i] = sigmoid_spec(a.logits[t * a.E + e]);
-                key[i] = __fadd_rn(s[i], a.bias ? a.bias[e] : 0.0f);
-                avail |= 1u << i;
-            }
-        }
-        int sel_e[MM_MAX_TOPK];
-        float sel_s[MM_MAX_TOPK];
-#pragma unroll
-        for (int j = 0; j < MM_MAX_TOPK; ++j) {
-            if (j >= a.k) break;
-            float bk = -INFINITY, bs = 0.0f;
-            int be = 0x7FFFFFFF;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                if (((avail >> i) & 1u) && (be == 0x7FFFFFFF || key[i] > bk)) {
-                    bk = key[i];
-                    bs = s[i];
-                    be = lane + 32 * i;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
-                const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-                if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ok > bk || (ok == bk && oe < be))) {
-                    bk = ok;
-                    bs = os;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
-            sel_e[j] = be;
-            sel_s[j] = bs;
-        }
-        if (lane == 0) {
-            float S = sel_s[0];
-            for (int j = 1; j < a.k; ++j) S = __fadd_rn(S, sel_s[j]);
-            for (int j = 0; j < a.k; ++j) {
-                const int e = sel_e[j];
-                const int slot = static_cast<int>((t + j) % a.rc[e]);
-                a.idx[t * a.k + j] = e;
-                a.w[t * a.k + j] = __fdiv_rn(sel_s[j], S);
-                a.phys[t * a.k + j] = a.map[static_cast<int64_t>(e) * a.R + slot];
-                if (a.counts) atomicAdd(&hist[e], 1);
-            }
-        }
-    }
+    if (t < a.T) route_token_any(a, t, threadIdx.x & 31, hist);
     if (a.counts) {
         __syncthreads();
         for (int e = threadIdx.x; e < a.E; e += blockDim.x)
@@ -273,44 +162,8 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(const __nv_bfloat16
     const int nb = H / 32;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = g / nb;
-    const int b = static_cast<int>(g % nb);
     if (t >= T) return;
-    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + b * 32);
-    float v[32];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 u = __ldg(src + q);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[q * 8 + 2 * i] = __uint_as_float(w4[i] << 16);
-            v[q * 8 + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-        }
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const int X = mx_e4m3_exponent(amax);
-    const float inv = exp2i(-X);
-    uint32_t packed[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t wd = 0;
-        if (amax > 0.0f) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) wd |= e4m3_code(v[4 * i + j], inv) << (8 * j);
-        }
-        packed[i] = wd;
-    }
-    const uint8_t sbyte = static_cast<uint8_t>(X + 127);
-    const int kchunks = H / 128;
-    for (int j = 0; j < k; ++j) {
-        const int64_t row = pos[t * k + j];
-        uint4* dst = reinterpret_cast<uint4*>(xq + row * H + b * 32);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        xs_t[sf_tile_offset(row, b, kchunks)] = sbyte;
-    }
+    quant_dispatch_block(x, t, static_cast<int>(g % nb), H, k, pos + t * k, xq, xs_t);
 }
 
 // ---------------------------------------------------------------------------
@@ -324,29 +177,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     const int nc = H / 8;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = g / nc;
-    const int c = static_cast<int>(g % nc);
     if (t >= T) return;
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-        const float wj = w[t * k + j];
-        const int64_t row = pos[t * k + j];
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(y + row * H) + c);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(wj, __uint_as_float(w4[i] << 16), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(wj, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
-        }
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        o[i] = *reinterpret_cast<const uint32_t*>(&b2);
-    }
-    reinterpret_cast<uint4*>(out + t * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    combine_chunk(y, w, pos, t, static_cast<int>(g % nc), H, k, out);
 }
 
 __global__ void tile_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K)
@@ -378,11 +210,7 @@ cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias
     a.E = c->E;
     a.k = c->k;
     a.R = c->R;
-    const unsigned grid = grid_for(T, kRouteWarps);
-    const int vpl = (c->E + 31) / 32;
-    if (vpl <= 4) route_kernel<4><<<grid, kRouteWarps * 32, 0, s>>>(a);
-    else if (vpl <= 8) route_kernel<8><<<grid, kRouteWarps * 32, 0, s>>>(a);
-    else route_kernel<16><<<grid, kRouteWarps * 32, 0, s>>>(a);
+    route_kernel<<<grid_for(T, kRouteWarps), kRouteWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 

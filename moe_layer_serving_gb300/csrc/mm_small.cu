@@ -1,0 +1,298 @@
+// mm_small.cu -- the fused small-input kernel of the MoE forward (T <= 512):
+// one cooperative launch, one CTA per SM, runs every stage of the layer
+// ("one kernel for quant, dispatch, GEMM1, GEMM2 and combine", sglang PR
+// #47065, Title/switches):
+//
+//   A  route + fused EPLB remap + count recording      (one warp per token)
+//      -- grid barrier --
+//   C  permute: every CTA rebuilds the expert segments, token tiles and the
+//      stable dispatch rows in shared memory from the T*k physical ids
+//   D  MXFP8 quantisation + dispatch copy               (one thread per block)
+//      -- grid barrier --
+//   F  GEMM1 (+SwiGLU, requant) and GEMM2 units, weight-streaming tcgen05
+//      pipeline; a GEMM2 unit waits only for the GEMM1 units of its tile
+//      -- grid barrier --
+//   H  weighted combine                                  (one thread per 8 outputs)
+//
+// Every grid barrier and every wait is bounded; a timeout latches
+// MM_ERR_TIMEOUT with its site, the remaining stages are skipped and the
+// tensor memory is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "mm_gemm.cuh"
+#include "mm_stages.cuh"
+
+namespace mm {
+namespace {
+
+constexpr int kSmallWarps = kThreads / 32;
+constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
+constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kTile;
+constexpr int kSmallSmemBytes = kGemmSmemBytes + 3 * kMaxSmallTiles * 4 + 64 + 1024;
+
+struct SmallArgs {
+    RouteArgs route;
+    const __nv_bfloat16* x;   // hidden [T, H]
+    __nv_bfloat16* out;       // [T, H]
+    int32_t* pos;             // [T*k] dispatch rows (global copy)
+    int32_t* off;             // [P+1]
+    int32_t* tile_expert;     // global copies of the tile table (debug, combine)
+    int32_t* tile_row0;
+    int32_t* tile_rows;
+    int32_t* num_tiles;
+    uint8_t* xq;              // dispatched activation codes [rows, H]
+    uint8_t* xs_t;            // their scale tiles
+    unsigned* bar;            // grid barrier {count, generation}
+    int P;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Sense-counting grid barrier: the last CTA to arrive resets the count and
+// bumps the generation; the others wait (bounded) for the bump.
+__device__ bool grid_sync(unsigned* bar, int* status, volatile int* abort_flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0 && !*abort_flag) {
+        const unsigned gen = ld_acquire_u32(bar + 1);
+        __threadfence();
+        if (atomicAdd(bar, 1u) + 1u == gridDim.x) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_u32(bar + 1) == gen) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    latch_error(status, MM_ERR_TIMEOUT, kSiteGridBarrier);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return !*abort_flag;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    small_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g,
+                 const __grid_constant__ SmallArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const GemmSmem s = gemm_smem(smem);
+    int* t_expert = reinterpret_cast<int*>(smem + kGemmSmemBytes);
+    int* t_row0 = t_expert + kMaxSmallTiles;
+    int* t_rows = t_row0 + kMaxSmallTiles;
+    int* scal = t_rows + kMaxSmallTiles;            // [0] tiles, [1] rows
+    const uint32_t tmem = gemm_setup(s, maps);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t T = a.route.T;
+    const int k = a.route.k, P = a.P, H = g.H;
+    const int N = static_cast<int>(T) * k;
+
+    // ---- A: route + EPLB remap + record ----------------------------------
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kSmallWarps + warp; t < T;
+         t += static_cast<int64_t>(gridDim.x) * kSmallWarps)
+        route_token_any(a.route, t, lane, nullptr);
+
+    bool ok = grid_sync(a.bar, g.status, s.abort_flag);
+
+    // ---- C: permute, redundantly per CTA, in the (idle) pipeline buffers ----
+    int* sphys = reinterpret_cast<int*>(s.stages);          // [N]
+    int* spos = sphys + kMaxSmallPairs;                      // [N]
+    int* wcnt = spos + kMaxSmallPairs;                       // [warps][P]: counts, then running bases
+    int* cnt = wcnt + kSmallWarps * MM_MAX_EXPERTS;          // [P]
+    int* soff = cnt + MM_MAX_EXPERTS;                        // [P+1]
+    int* stoff = soff + MM_MAX_EXPERTS + 1;                  // [P]
+    const int chunk = ((N + kSmallWarps - 1) / kSmallWarps + 31) & ~31;
+    const int lo = min(N, warp * chunk), hi = min(N, lo + chunk);
+    const uint32_t lt = (1u << lane) - 1u;
+    if (ok) {
+        for (int i = threadIdx.x; i < N; i += kThreads) sphys[i] = a.route.phys[i];
+        for (int i = threadIdx.x; i < kSmallWarps * P; i += kThreads) wcnt[(i / P) * MM_MAX_EXPERTS + i % P] = 0;
+        __syncthreads();
+        int* wc = wcnt + warp * MM_MAX_EXPERTS;
+        for (int base = lo; base < hi; base += 32) {
+            const int i = base + lane;
+            const int p = i < hi ? sphys[i] : -1;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
+            if (p >= 0 && lane == __ffs(peers) - 1) wc[p] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        for (int p = threadIdx.x; p < P; p += kThreads) {
+            int run = 0;
+            for (int w = 0; w < kSmallWarps; ++w) {
+                const int v = wcnt[w * MM_MAX_EXPERTS + p];
+                wcnt[w * MM_MAX_EXPERTS + p] = run;
+                run += v;
+            }
+            cnt[p] = run;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive scans over experts of the padded segment sizes and tile counts
+            const int per = (P + 31) / 32;
+            const int p0 = lane * per, p1 = min(P, p0 + per);
+            int rows = 0, tiles = 0;
+            for (int p = p0; p < p1; ++p) {
+                rows += (cnt[p] + kTile - 1) / kTile * kTile;
+                tiles += (cnt[p] + kTile - 1) / kTile;
+            }
+            int rx = rows, tx = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int r = __shfl_up_sync(0xFFFFFFFFu, rx, o);
+                const int q = __shfl_up_sync(0xFFFFFFFFu, tx, o);
+                if (lane >= o) {
+                    rx += r;
+                    tx += q;
+                }
+            }
+            int ro = rx - rows, to = tx - tiles;
+            for (int p = p0; p < p1; ++p) {
+                soff[p] = ro;
+                stoff[p] = to;
+                ro += (cnt[p] + kTile - 1) / kTile * kTile;
+                to += (cnt[p] + kTile - 1) / kTile;
+            }
+            if (lane == 31) {
+                soff[P] = rx;
+                scal[0] = tx;
+                scal[1] = rx;
+            }
+        }
+        __syncthreads();
+        for (int p = threadIdx.x; p < P; p += kThreads) {
+            const int nt = (cnt[p] + kTile - 1) / kTile;
+            for (int t = 0; t < nt; ++t) {
+                t_expert[stoff[p] + t] = p;
+                t_row0[stoff[p] + t] = soff[p] + t * kTile;
+                t_rows[stoff[p] + t] = min(kTile, cnt[p] - t * kTile);
+            }
+        }
+        for (int base = lo; base < hi; base += 32) {
+            const int i = base + lane;
+            const int p = i < hi ? sphys[i] : -1;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
+            int before = 0;
+            if (p >= 0) {
+                before = wc[p];
+                spos[i] = soff[p] + before + __popc(peers & lt);
+            }
+            __syncwarp();
+            if (p >= 0 && lane == __ffs(peers) - 1) wc[p] = before + __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        if (blockIdx.x == 0) {
+            for (int i = threadIdx.x; i < N; i += kThreads) a.pos[i] = spos[i];
+            for (int p = threadIdx.x; p <= P; p += kThreads) a.off[p] = soff[p];
+            for (int t = threadIdx.x; t < scal[0]; t += kThreads) {
+                a.tile_expert[t] = t_expert[t];
+                a.tile_row0[t] = t_row0[t];
+                a.tile_rows[t] = t_rows[t];
+                g.done1[t] = 0;
+            }
+            if (threadIdx.x == 0) *a.num_tiles = scal[0];
+        }
+
+        // ---- D: MXFP8 quantisation + dispatch ------------------------------
+        const int nb = H / 32;
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < T * nb;
+             it += static_cast<int64_t>(gridDim.x) * kThreads) {
+            const int64_t t = it / nb;
+            quant_dispatch_block(a.x, t, static_cast<int>(it % nb), H, k, spos + t * k, a.xq, a.xs_t);
+        }
+        fence_proxy_async_global();
+    }
+    fence_proxy_async_shared();     // scratch writes above precede the TMA writes into the same buffers
+    ok = grid_sync(a.bar, g.status, s.abort_flag);
+
+    // ---- F: GEMM1 + SwiGLU + requant, GEMM2 (tiles from shared memory) -----
+    if (ok) {
+        TileView tv;
+        tv.expert = t_expert;
+        tv.row0 = t_row0;
+        tv.rows = t_rows;
+        tv.ntiles = scal[0];
+        gemm_roles(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+    }
+    gemm_teardown(tmem);
+    ok = grid_sync(a.bar, g.status, s.abort_flag);
+
+    // ---- H: combine ---------------------------------------------------------
+    if (ok) {
+        const int nc = H / 8;
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < T * nc;
+             it += static_cast<int64_t>(gridDim.x) * kThreads)
+            combine_chunk(g.y, a.route.w, a.pos, it / nc, static_cast<int>(it % nc), H, k, a.out);
+    }
+}
+
+}  // namespace
+}  // namespace mm
+
+namespace mm {
+
+cudaError_t small_prepare()
+{
+    return cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallSmemBytes);
+}
+
+cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logits, const float* bias, void* out,
+                         int64_t T, cudaStream_t s)
+{
+    GemmArgs g;
+    fill_gemm_args(c, &g);
+    SmallArgs a;
+    a.route.logits = logits;
+    a.route.bias = bias;
+    a.route.map = c->map;
+    a.route.rc = c->rc;
+    a.route.idx = c->idx;
+    a.route.w = c->wgt;
+    a.route.phys = c->phys;
+    a.route.counts = c->recording ? c->counts + static_cast<int64_t>(c->layer) * c->E : nullptr;
+    a.route.T = T;
+    a.route.E = c->E;
+    a.route.k = c->k;
+    a.route.R = c->R;
+    a.x = static_cast<const __nv_bfloat16*>(hidden);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.pos = c->pos;
+    a.off = c->off;
+    a.tile_expert = c->tile_expert;
+    a.tile_row0 = c->tile_row0;
+    a.tile_rows = c->tile_rows;
+    a.num_tiles = c->num_tiles;
+    a.xq = c->xq;
+    a.xs_t = c->xs_t;
+    a.bar = c->grid_bar;
+    a.P = c->P;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c->sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmallSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, small_kernel, c->maps, g, a);
+}
+
+}  // namespace mm

@@ -1,0 +1,215 @@
+// mm_stages.cuh -- per-item bodies of the SIMT stages of the fused MoE
+// forward (route one token, quantise + dispatch one 32-element block, combine
+// one 8-element output chunk).  The standalone kernels and the fused
+// small-input kernel call the same bodies.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "mm_device.cuh"
+#include "mm_internal.h"
+
+namespace mm {
+
+// ---------------------------------------------------------------------------
+// routing score: a fixed binary32 operation sequence (Cody-Waite reduction
+// with a two-part ln 2, degree-7 Taylor polynomial in Horner form, 2^n by the
+// exponent field), every step one IEEE-rounded add, mul or div and no fused
+// multiply-add, so the score -- and with it the selected experts -- is the
+// same on every machine that evaluates this sequence.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float exp_spec(float y)
+{
+    const float log2e = __uint_as_float(0x3FB8AA3Bu);
+    const float ln2_hi = __uint_as_float(0x3F317200u);
+    const float ln2_lo = __uint_as_float(0x35BFBE8Eu);
+    const float c2 = __uint_as_float(0x3F000000u);  // 1/2
+    const float c3 = __uint_as_float(0x3E2AAAABu);  // 1/6
+    const float c4 = __uint_as_float(0x3D2AAAABu);  // 1/24
+    const float c5 = __uint_as_float(0x3C088889u);  // 1/120
+    const float c6 = __uint_as_float(0x3AB60B61u);  // 1/720
+    const float c7 = __uint_as_float(0x39500D01u);  // 1/5040
+    y = fminf(fmaxf(y, -87.0f), 88.0f);
+    const float n = rintf(__fmul_rn(y, log2e));
+    float r = __fsub_rn(y, __fmul_rn(n, ln2_hi));
+    r = __fsub_rn(r, __fmul_rn(n, ln2_lo));
+    float p = c7;
+    p = __fadd_rn(__fmul_rn(p, r), c6);
+    p = __fadd_rn(__fmul_rn(p, r), c5);
+    p = __fadd_rn(__fmul_rn(p, r), c4);
+    p = __fadd_rn(__fmul_rn(p, r), c3);
+    p = __fadd_rn(__fmul_rn(p, r), c2);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    return __fmul_rn(p, exp2i(static_cast<int>(n)));
+}
+
+__device__ __forceinline__ float sigmoid_spec(float x)
+{
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_spec(-x)));
+}
+
+struct RouteArgs {
+    const float* logits;   // [T, E]
+    const float* bias;     // [E] or null
+    const int32_t* map;    // [E, R]
+    const int32_t* rc;     // [E]
+    int32_t* idx;          // [T, k]
+    float* w;              // [T, k]
+    int32_t* phys;         // [T, k]
+    int64_t* counts;       // [E] of the bound layer, or null when not recording
+    int64_t T;
+    int E, k, R;
+};
+
+// One warp routes token t: lane l holds experts l, l+32, ...; k rounds of a
+// warp arg-max over (key, -expert) select the experts in order, ties to the
+// lower expert index.  Lane 0 writes idx/w/phys and counts the selections:
+// into shared memory (hist != null) or straight into the global table.
+template <int VPL>
+__device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int lane, int* hist)
+{
+    float s[VPL], key[VPL];
+    uint32_t avail = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        s[i] = 0.0f;
+        key[i] = 0.0f;
+        if (e < a.E) {
+            s[i] = sigmoid_spec(a.logits[t * a.E + e]);
+            key[i] = __fadd_rn(s[i], a.bias ? a.bias[e] : 0.0f);
+            avail |= 1u << i;
+        }
+    }
+    int sel_e[MM_MAX_TOPK];
+    float sel_s[MM_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MM_MAX_TOPK; ++j) {
+        if (j >= a.k) break;
+        float bk = -INFINITY, bs = 0.0f;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            if (((avail >> i) & 1u) && (be == 0x7FFFFFFF || key[i] > bk)) {
+                bk = key[i];
+                bs = s[i];
+                be = lane + 32 * i;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
+            const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+            if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ok > bk || (ok == bk && oe < be))) {
+                bk = ok;
+                bs = os;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+        sel_e[j] = be;
+        sel_s[j] = bs;
+    }
+    if (lane == 0) {
+        float S = sel_s[0];
+        for (int j = 1; j < a.k; ++j) S = __fadd_rn(S, sel_s[j]);
+        for (int j = 0; j < a.k; ++j) {
+            const int e = sel_e[j];
+            const int slot = static_cast<int>((t + j) % a.rc[e]);
+            a.idx[t * a.k + j] = e;
+            a.w[t * a.k + j] = __fdiv_rn(sel_s[j], S);
+            a.phys[t * a.k + j] = a.map[static_cast<int64_t>(e) * a.R + slot];
+            if (a.counts) {
+                if (hist) atomicAdd(&hist[e], 1);
+                else atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + e), 1ull);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void route_token_any(const RouteArgs& a, int64_t t, int lane, int* hist)
+{
+    const int vpl = (a.E + 31) / 32;
+    if (vpl <= 4) route_token<4>(a, t, lane, hist);
+    else if (vpl <= 8) route_token<8>(a, t, lane, hist);
+    else route_token<16>(a, t, lane, hist);
+}
+
+// MXFP8 quantisation of block b (32 elements) of token t and its dispatch to
+// the token's k rows: 4 x 128-bit loads, one e8m0 scale, 32 e4m3 codes per
+// row (2 x 128-bit stores).  pos_t points at the k dispatch rows of token t.
+__device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
+                                                     int k, const int32_t* pos_t, uint8_t* __restrict__ xq,
+                                                     uint8_t* __restrict__ xs_t)
+{
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + b * 32);
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(src + q);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[q * 8 + 2 * i] = __uint_as_float(w4[i] << 16);
+            v[q * 8 + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int X = mx_e4m3_exponent(amax);
+    const float inv = exp2i(-X);
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t wd = 0;
+        if (amax > 0.0f) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wd |= e4m3_code(v[4 * i + j], inv) << (8 * j);
+        }
+        packed[i] = wd;
+    }
+    const uint8_t sbyte = static_cast<uint8_t>(X + 127);
+    const int kchunks = H / 128;
+    for (int j = 0; j < k; ++j) {
+        const int64_t row = pos_t[j];
+        uint4* dst = reinterpret_cast<uint4*>(xq + row * H + b * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        xs_t[sf_tile_offset(row, b, kchunks)] = sbyte;
+    }
+}
+
+// out[t][8c .. 8c+8) = bf16( sum_j w[t,j] * y[pos[t,j]][...] ), fp32, j in order.
+__device__ __forceinline__ void combine_chunk(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w,
+                                              const int32_t* __restrict__ pos, int64_t t, int c, int H, int k,
+                                              __nv_bfloat16* __restrict__ out)
+{
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        const float wj = w[t * k + j];
+        const int64_t row = pos[t * k + j];
+        const uint4 u = *(reinterpret_cast<const uint4*>(y + row * H) + c);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj, __uint_as_float(w4[i] << 16), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    reinterpret_cast<uint4*>(out + t * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+}  // namespace mm

@@ -74,10 +74,14 @@ def test_forced_routes_agree(torch):
     hidden, logits, bias = synthetic.make_activations(cfg, 200)
     run = gpu_util.Run(cfg, cap=200)
     outs = []
-    for r in (mm.ROUTE_SMALL, mm.ROUTE_LARGE, mm.ROUTE_AUTO):
+    for r, expect in ((mm.ROUTE_SMALL, (1, 1)), (mm.ROUTE_LARGE, (2, 7)), (mm.ROUTE_AUTO, (1, 1))):
         run.op.set_route(r)
         outs.append(run.forward(hidden, logits, bias, dumps=False)["out"])
+        route, launches, site = run.op.last_info()
+        assert (route, launches) == expect and site == 0
     run.close()
+    # the fused small-input kernel and the multi-kernel large-input path agree bit for bit
+    assert np.array_equal(outs[0], outs[1])
     ref = oracle.forward(hidden, logits, bias, cfg.k, gpu_util.weights(cfg))["out"]
     for o in outs:
         gpu_util.assert_out_close(o, ref)
