@@ -6,9 +6,9 @@
  * recording, MXFP8 activation quantisation, dispatch into expert-sorted
  * tiles, GEMM1 (gate/up) with a SwiGLU + MXFP8 requantisation epilogue,
  * GEMM2 (down) and the top-k weighted combine.  Sources for the operation:
- *   - "sglang PR #47065" (Title/switches, Modifications): the operator is
- *     one kernel for "quant, dispatch, GEMM1, GEMM2 and combine", with a
- *     small-input path (up to 512 tokens) and a persistent large-input path
+ *   - "sglang PR #47065" (Title/switches, Modifications): quantisation,
+ *     dispatch, both expert GEMMs and the combine form one operator, with a
+ *     single-kernel small-input path (up to 512 tokens) and a persistent large-input path
  *     (>= 1024 tokens), a per-layer slot (bind_layer) and a three-state
  *     large-input switch;
  *   - "sglang PR #35619" (Summary, EPLB arm settings): fused EPLB remap and

@@ -1,7 +1,7 @@
 // mm_small.cu -- the fused small-input kernel of the MoE forward (T <= 512):
 // one cooperative launch, one CTA per SM, runs every stage of the layer
-// ("one kernel for quant, dispatch, GEMM1, GEMM2 and combine", sglang PR
-// #47065, Title/switches):
+// (the pages' small-input path runs quantisation, dispatch, both expert GEMMs
+// and the combine as a single kernel, "sglang PR #47065", Title/switches):
 //
 //   A  route + fused EPLB remap + count recording      (one warp per token)
 //      -- grid barrier --

@@ -6,8 +6,8 @@
  * CPU-baseline leg do.  It shares no code with the CUDA library.
  *
  * What it computes, stage by stage (the pages name the stages of the fused
- * operator -- "quant, dispatch, GEMM1, GEMM2 and combine" -- in "sglang PR
- * #47065", Title/switches; the fused EPLB remap and per-expert load recording
+ * operator -- activation quantisation, dispatch, the two expert GEMMs and the
+ * combine, in one kernel -- in "sglang PR #47065", Title/switches; the fused EPLB remap and per-expert load recording
  * in "sglang PR #35619", Summary; a8w4 with MXFP4 routed experts in
  * "InferenceX PR #3430", draft-precision notes):
  *
