@@ -190,6 +190,30 @@ MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);
 MM_API mm_status mm_profile_begin(mm_handle h, int max_launches);
 MM_API mm_status mm_profile_end(mm_handle h, float *ms_out, int max_out, int *n_out);
 
+/* Dispatch plan without allocation.  The pages have no counterpart; this is a
+ * convenience for callers that cannot allocate device memory where they need
+ * the plan (code running under another framework's memory pool or an
+ * allocator-free runtime, or a steady-state serving loop that must not call
+ * cudaMalloc, which synchronises the device).
+ *
+ * Inputs (device pointers): phys [npairs] int32, the physical expert of each
+ * (token, slot) pair in pair order; num_physical P (1..512).  Outputs (device
+ * pointers): pos [npairs] int32, the dispatch row of each pair, and offsets
+ * [P + 1] int32, each expert's segment start -- the same plan mm_forward's
+ * permute builds: pairs grouped by expert in pair order, segments padded to
+ * multiples of 128 rows, offsets[P] = total rows.  An id outside [0, P) gets
+ * pos = -1 and is left out.  npairs <= 131072, else MM_ERR_CAPACITY.
+ *
+ * Scratch lives in a 256 KB array inside the library, not in allocated
+ * memory; every GPU that loads the library holds it until the process exits.
+ * The first call on a device looks up that array's device address (make it
+ * before any stream capture).  All calls share the array, so calls whose
+ * kernels overlap on the GPU (different streams, or different threads without
+ * ordering) race and must not be made; calls in one stream are fine.
+ * Asynchronous on `stream`; allocates nothing. */
+MM_API mm_status mm_plan_dispatch_static(const int32_t *phys, int64_t npairs, int num_physical, int32_t *pos,
+                                         int32_t *offsets, mm_stream stream);
+
 /* Short text for a status code (static storage). */
 MM_API const char *mm_status_string(mm_status s);
 

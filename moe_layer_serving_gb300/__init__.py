@@ -47,6 +47,7 @@ _SIGS = {
     "mm_debug_size": [_p, _i32, C.POINTER(_sz)],
     "mm_profile_begin": [_p, _i32],
     "mm_profile_end": [_p, _p, _i32, C.POINTER(_i32)],
+    "mm_plan_dispatch_static": [_p, _i64, _i32, _p, _p, _p],
 }
 _lib = None
 
