@@ -163,7 +163,7 @@ MM_API mm_status mm_get_status(mm_handle h, int *device_code);
  *   2 phys    int32 [T, k]     physical experts
  *   3 pos     int32 [T, k]     dispatch row of each (token, slot) pair
  *   4 offsets int32 [P + 1]    start row of each physical expert's segment
- *                              (segments are padded to 128 rows); [P] = total
+ *                              (segments are padded to 16 rows); [P] = total
  *   5 xq      uint8 [rows, H]  dispatched MXFP8 activation codes
  *   6 xs      uint8 [rows, H/32] their scale bytes, row-major
  *   7 hq      uint8 [rows, I]  GEMM1 output codes (after SwiGLU, requant)
@@ -175,7 +175,10 @@ MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t by
 
 /* Stage 10 of mm_debug_dump: int32 [3] = {route taken by the last forward
  * (1 small, 2 large), number of kernels it launched, site of the last
- * device-side timeout (0 none; see WaitSite in the sources)}. */
+ * device-side timeout (0 none; see WaitSite in the sources)}.
+ * Stage 11: uint64 [SMs][8] %globaltimer readings (ns) of each CTA of the last
+ * fused small-input launch at its stage boundaries: start, routed, past
+ * barrier 1, dispatched, past barrier 2, GEMMs done, past barrier 3, end. */
 
 /* Size in bytes of a debug stage for the last forward (0 before any). */
 MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);
@@ -201,7 +204,7 @@ MM_API mm_status mm_profile_end(mm_handle h, float *ms_out, int max_out, int *n_
  * pointers): pos [npairs] int32, the dispatch row of each pair, and offsets
  * [P + 1] int32, each expert's segment start -- the same plan mm_forward's
  * permute builds: pairs grouped by expert in pair order, segments padded to
- * multiples of 128 rows, offsets[P] = total rows.  An id outside [0, P) gets
+ * multiples of 16 rows, offsets[P] = total rows.  An id outside [0, P) gets
  * pos = -1 and is left out.  npairs <= 131072, else MM_ERR_CAPACITY.
  *
  * Scratch lives in a 256 KB array inside the library, not in allocated

@@ -48,6 +48,20 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t cols,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weight tiles [nblocks][128 rows][128 e2m1], one 8 KB box per (row block, K block).
+bool make_weight_map(CUtensorMap* m, void* base, uint64_t nblocks)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, 128, nblocks};
+    const cuuint64_t strides[2] = {64, 8192};
+    const cuuint32_t box[3] = {128, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int env_int(const char* name, int dflt)
@@ -197,13 +211,13 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
             return MM_ERR_CUDA;
         }
     }
-    CK(cudaMemcpy(c->w1, w1, n_w1, cudaMemcpyDeviceToDevice));
-    CK(cudaMemcpy(c->w2, w2, n_w2, cudaMemcpyDeviceToDevice));
+    CK(mm::launch_tile_weights(w1, c->w1, static_cast<int64_t>(P * 2 * I), c->H, nullptr));
+    CK(mm::launch_tile_weights(w2, c->w2, static_cast<int64_t>(P * H), c->I, nullptr));
     CK(mm::launch_tile_scales(w1s, c->w1_sf, static_cast<int64_t>(P * 2 * I), c->H, nullptr));
     CK(mm::launch_tile_scales(w2s, c->w2_sf, static_cast<int64_t>(P * H), c->I, nullptr));
     CK(cudaDeviceSynchronize());
-    if (!make_map(&c->maps.w1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, c->w1, H, P * 2 * I, H / 2, kTile) ||
-        !make_map(&c->maps.w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, c->w2, I, P * H, I / 2, kTile))
+    if (!make_weight_map(&c->maps.w1, c->w1, (P * 2 * I / kTile) * (H / 128)) ||
+        !make_weight_map(&c->maps.w2, c->w2, (P * H / kTile) * (I / 128)))
         return MM_ERR_CUDA;
     c->maps_weights = true;
     c->weights_set = true;
@@ -279,8 +293,10 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     if (max_tokens <= c->cap_tokens) return MM_OK;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
     const int64_t npairs = max_tokens * c->k;
-    const int64_t rows = (npairs + static_cast<int64_t>(c->P) * (kTile - 1) + kTile - 1) / kTile * kTile;
-    const int64_t tiles = rows / kTile;
+    // each non-empty segment adds < kSegAlign pad rows and < 1 partial token tile
+    const int64_t busy = npairs < c->P ? npairs : c->P;
+    const int64_t rows = npairs + busy * (mm::kSegAlign - 1) + mm::kSegAlign;
+    const int64_t tiles = npairs / mm::kTileN + busy + 1;
     const int64_t chunks = (npairs + mm::kChunkPairs - 1) / mm::kChunkPairs;
     const int64_t H = c->H, I = c->I;
     // size pass, then carve
@@ -289,13 +305,15 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     add(npairs * 4 * 4);                      // idx, phys, pos, wgt
     add(chunks * c->P * 4);
     add((c->P + 1) * 4);
+    add(c->P * 4);                            // first tile of each expert
     add(tiles * 4 * 4 + 4);                   // tile table, done1, num_tiles
     add(rows * H);
-    add(rows * H / 32);
+    add(tiles * (H / 128) * 512);
     add(rows * I);
-    add(rows * I / 32);
+    add(tiles * (I / 128) * 512);
     add(rows * H * 2);
     add(64);                                  // grid barrier
+    add(static_cast<size_t>(c->sms) * 8 * 8); // stage timestamps
     bytes += 8 * 256;
     cudaDeviceSynchronize();
     free_ws(c);
@@ -312,17 +330,19 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->wgt = carve<float>(p, npairs);
     c->chunk_hist = carve<int32_t>(p, chunks * c->P);
     c->off = carve<int32_t>(p, c->P + 1);
+    c->toff = carve<int32_t>(p, c->P);
     c->tile_expert = carve<int32_t>(p, tiles);
     c->tile_row0 = carve<int32_t>(p, tiles);
     c->tile_rows = carve<int32_t>(p, tiles);
     c->done1 = carve<int32_t>(p, tiles);
     c->num_tiles = carve<int32_t>(p, 1);
     c->xq = carve<uint8_t>(p, rows * H);
-    c->xs_t = carve<uint8_t>(p, rows * H / 32);
+    c->xs_t = carve<uint8_t>(p, tiles * (H / 128) * 512);
     c->hq = carve<uint8_t>(p, rows * I);
-    c->hs_t = carve<uint8_t>(p, rows * I / 32);
+    c->hs_t = carve<uint8_t>(p, tiles * (I / 128) * 512);
     c->y = carve<__nv_bfloat16>(p, rows * H);
     c->grid_bar = carve<unsigned>(p, 16);
+    c->stamps = carve<uint64_t>(p, static_cast<size_t>(c->sms) * 8);
     c->ws = ws;
     c->ws_bytes = bytes;
     if (!make_map(&c->maps.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox) ||
@@ -455,6 +475,7 @@ static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* 
         case 8: *bytes = static_cast<size_t>(rows) * c->I / 32; break;
         case 9: *bytes = static_cast<size_t>(rows) * c->H * 2; break;
         case 10: *bytes = 3 * sizeof(int32_t); break;
+        case 11: *bytes = static_cast<size_t>(c->sms) * 8 * sizeof(uint64_t); break;
         default: return MM_ERR_INVALID_ARG;
     }
     return MM_OK;
@@ -493,24 +514,34 @@ mm_status mm_debug_dump(mm_handle c, int stage, void* dst, size_t bytes)
         case 5: src = c->xq; break;
         case 7: src = c->hq; break;
         case 9: src = c->y; break;
+        case 11: src = c->stamps; break;
         default: break;
     }
     if (src) {
         CK(cudaMemcpy(dst, src, n, cudaMemcpyDeviceToHost));
         return MM_OK;
     }
-    // scale stages: un-tile into row-major [rows][K/32]
+    // scale stages: per-token-tile scale tiles -> row-major [rows][K/32] (pad rows 0)
     const int K = stage == 6 ? c->H : c->I;
-    const uint8_t* tiled = stage == 6 ? c->xs_t : c->hs_t;
-    std::vector<uint8_t> t(full);
-    CK(cudaMemcpy(t.data(), tiled, full, cudaMemcpyDeviceToHost));
-    uint8_t* d = static_cast<uint8_t*>(dst);
     const int nb = K / 32;
-    for (int64_t r = 0; r < rows; ++r)
-        for (int b = 0; b < nb; ++b) {
-            const size_t at = static_cast<size_t>(r) * nb + b;
-            if (at < n) d[at] = t[mm::sf_tile_offset(r, b, K / 128)];
-        }
+    const uint8_t* tiled = stage == 6 ? c->xs_t : c->hs_t;
+    int32_t ntiles = 0;
+    CK(cudaMemcpy(&ntiles, c->num_tiles, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    std::vector<int32_t> row0(ntiles), trows(ntiles);
+    std::vector<uint8_t> t(static_cast<size_t>(ntiles) * (K / 128) * 512);
+    if (ntiles > 0) {
+        CK(cudaMemcpy(row0.data(), c->tile_row0, ntiles * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CK(cudaMemcpy(trows.data(), c->tile_rows, ntiles * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CK(cudaMemcpy(t.data(), tiled, t.size(), cudaMemcpyDeviceToHost));
+    }
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    memset(d, 0, n);
+    for (int32_t tile = 0; tile < ntiles; ++tile)
+        for (int r = 0; r < trows[tile]; ++r)
+            for (int b = 0; b < nb; ++b) {
+                const size_t at = static_cast<size_t>(row0[tile] + r) * nb + b;
+                if (at < n) d[at] = t[mm::act_sf_offset(tile, r, b, K / 128)];
+            }
     return MM_OK;
 }
 

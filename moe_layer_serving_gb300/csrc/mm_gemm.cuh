@@ -4,7 +4,7 @@
 //
 // Both GEMMs run "weights as A": the MMA's M = 128 weight rows (e2m1, the
 // packed MXFP4 operand, unpacked to one byte per element in shared memory by
-// the TMA), N = up to 128 dispatched token rows of one physical expert (e4m3),
+// the TMA), N = up to 112 dispatched token rows of one physical expert (e4m3),
 // K in stages of 128, one e8m0 scale per 32 along K for both operands
 // (tcgen05.mma kind::mxf8f6f4 block_scale, fp32 accumulators in tensor memory).
 //
@@ -34,8 +34,11 @@ namespace mm {
 constexpr int kThreads = 192;
 constexpr int kEpiWarp0 = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColSFA0 = 256, kColSFA1 = 260, kColSFB = 264;
-constexpr int kPrefetchSteps = 8;   // L2 look-ahead of the weight stream, in (unit, k-step) pairs
+// TMEM columns: two accumulator buffers of 2 x kTileN fp32 columns (one per A
+// tile), then the scale factors of the current stage.
+constexpr uint32_t kAccCols = 2 * kTileN;
+constexpr uint32_t kColSFA0 = 2 * kAccCols, kColSFA1 = kColSFA0 + 4, kColSFB = kColSFA0 + 8;
+static_assert(kColSFB + 4 <= kTmemCols, "accumulators and scale factors must fit in TMEM");
 
 struct Unit {
     int phase;      // 1 or 2
@@ -125,9 +128,9 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* smem)
     s.stages = smem;
     s.full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     s.empty = s.full + kStages;
-    s.tmem_full = s.empty + kStages;
-    s.tmem_empty = s.tmem_full + 1;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.tmem_empty + 1);
+    s.tmem_full = s.empty + kStages;      // [2], one per accumulator buffer
+    s.tmem_empty = s.tmem_full + 2;       // [2]
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.tmem_empty + 2);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
     return s;
 }
@@ -141,8 +144,10 @@ __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
         }
-        mbar_init(s.tmem_full, 1);
-        mbar_init(s.tmem_empty, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s.tmem_full[b], 1);
+            mbar_init(&s.tmem_empty[b], 128);
+        }
         *s.abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&maps.w1);
@@ -191,12 +196,6 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
             uint32_t phase = 0;
             int armed[kStages];
             for (int s = 0; s < kStages; ++s) armed[s] = -1;
-            // L2 look-ahead: weight tiles kPrefetchSteps (unit, k-step) pairs ahead of
-            // the loads, so that more weight bytes are in flight than the ring holds
-            Unit pf;
-            int pf_u = first_unit, pf_ks = 0;
-            bool pf_ok = decode_unit(g, tv, pf_u, pf);
-            int64_t issued = 0, loaded = 0;
             Unit un;
             for (int u = first_unit; decode_unit(g, tv, u, un) && !*abort_flag; u += unit_stride) {
                 const CUtensorMap* wmap = un.phase == 1 ? &maps.w1 : &maps.w2;
@@ -222,24 +221,14 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
                 const int nbox = un.n / kBBox;
                 const uint32_t bytes = un.na * kATileTxBytes + nbox * kBBox * kKStep + (un.na + 1) * kSFBytes;
                 for (int ks = 0; ks < un.ksteps; ++ks) {
-                    while (pf_ok && issued < loaded + kPrefetchSteps) {
-                        const CUtensorMap* pmap = pf.phase == 1 ? &maps.w1 : &maps.w2;
-                        for (int a = 0; a < pf.na; ++a) tma_prefetch_2d(pmap, pf_ks * kKStep, pf.arow[a]);
-                        ++issued;
-                        if (++pf_ks == pf.ksteps) {
-                            pf_ks = 0;
-                            pf_u += unit_stride;
-                            pf_ok = decode_unit(g, tv, pf_u, pf);
-                        }
-                    }
-                    ++loaded;
                     if (!mbar_wait(&empty[stage], phase ^ 1u, g.status, abort_flag, kSiteProducerEmpty)) break;
                     uint8_t* st = smem + stage * kStageBytes;
                     uint8_t* sf = st + 2 * kATileBytes + kBTileBytes;
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     armed[stage] = static_cast<int>(phase);
                     for (int a = 0; a < un.na; ++a) {
-                        tma_load_2d(st + a * kATileBytes, wmap, ks * kKStep, un.arow[a], &full[stage], pol_w);
+                        tma_load_3d(st + a * kATileBytes, wmap, 0, 0, un.sfrb[a] * un.ksteps + ks, &full[stage],
+                                    pol_w);
                         bulk_load(sf + a * kSFBytes, wsf + (static_cast<int64_t>(un.sfrb[a]) * un.ksteps + ks) * kSFBytes,
                                   kSFBytes, &full[stage]);
                     }
@@ -247,7 +236,7 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
                         tma_load_2d(st + 2 * kATileBytes + bx * kBBox * kKStep, amap, ks * kKStep,
                                     un.row0 + bx * kBBox, &full[stage], pol_a);
                     bulk_load(sf + 2 * kSFBytes,
-                              asf + (static_cast<int64_t>(un.row0 / kTile) * un.ksteps + ks) * kSFBytes, kSFBytes,
+                              asf + (static_cast<int64_t>(un.tile) * un.ksteps + ks) * kSFBytes, kSFBytes,
                               &full[stage]);
                     if (++stage == kStages) {
                         stage = 0;
@@ -269,10 +258,11 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            uint32_t phase = 0, acc_iter = 0;
             Unit un;
             for (int u = first_unit; decode_unit(g, tv, u, un) && !*abort_flag; u += unit_stride) {
-                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, g.status, abort_flag, kSiteMmaTmemEmpty)) break;
+                const uint32_t buf = acc_iter & 1u, acc_phase = (acc_iter >> 1) & 1u;
+                if (!mbar_wait(&tmem_empty[buf], acc_phase ^ 1u, g.status, abort_flag, kSiteMmaTmemEmpty)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < un.ksteps; ++ks) {
                     if (!mbar_wait(&full[stage], phase, g.status, abort_flag, kSiteMmaFull)) break;
@@ -288,7 +278,7 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
                         const uint32_t idesc = idesc_e2m1_e4m3(static_cast<uint32_t>(un.n), kk);
                         for (int a = 0; a < un.na; ++a) {
                             const uint64_t adesc = desc_kmajor_sw128(st + a * kATileBytes);
-                            mma_mxf8f6f4(tmem + a * kTile, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                            mma_mxf8f6f4(tmem + buf * kAccCols + a * kTileN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
                                          tmem + (a == 0 ? kColSFA0 : kColSFA1), tmem + kColSFB,
                                          (ks | kk) != 0 ? 1u : 0u);
                         }
@@ -300,14 +290,15 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
                     }
                 }
                 if (*abort_flag) break;
-                tc_commit(tmem_full);
-                acc_phase ^= 1u;
+                tc_commit(&tmem_full[buf]);
+                ++acc_iter;
             }
             if (*abort_flag) {
                 // drain issued tensor-core work before the allocation is freed
-                tc_commit(tmem_full);
+                const uint32_t buf = acc_iter & 1u, acc_phase = (acc_iter >> 1) & 1u;
+                tc_commit(&tmem_full[buf]);
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(tmem_full, acc_phase))
+                while (!mbar_try_wait(&tmem_full[buf], acc_phase))
                     if (globaltimer() - t0 > kWaitLimitNs / 4) break;
             }
         }
@@ -315,35 +306,49 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
         // --------------------------------------------------------------- epilogue
         const int q = warp & 3;                  // tensor-memory lane quarter of this warp
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        uint32_t acc_phase = 0;
+        uint32_t acc_iter = 0;
         Unit un;
         for (int u = first_unit; decode_unit(g, tv, u, un) && !*abort_flag; u += unit_stride) {
-            if (!mbar_wait(tmem_full, acc_phase, g.status, abort_flag, kSiteEpiTmemFull)) break;
+            const uint32_t buf = acc_iter & 1u, acc_phase = (acc_iter >> 1) & 1u;
+            const uint32_t acc = tmem + lane_base + buf * kAccCols;
+            if (!mbar_wait(&tmem_full[buf], acc_phase, g.status, abort_flag, kSiteEpiTmemFull)) break;
             tc_fence_after();
             if (un.phase == 1) {
                 const int col = un.blk * kTile + 32 * q + lane;   // column of h (I axis)
                 const int kchunks = g.I / kKStep;
                 for (int c0 = 0; c0 < un.n; c0 += 16) {
                     uint32_t gr[16], ur[16];
-                    tmem_ld_32x32b_x16(tmem + lane_base + c0, gr);
-                    tmem_ld_32x32b_x16(tmem + lane_base + kTile + c0, ur);
+                    tmem_ld_32x32b_x16(acc + c0, gr);
+                    tmem_ld_32x32b_x16(acc + kTileN + c0, ur);
                     tmem_ld_wait();
+                    // SwiGLU for 16 token columns, then their 16 warp-wide amax
+                    // reductions interleaved, then codes; columns past the tile's
+                    // rows are computed but not stored
+                    float h[16], am[16];
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
-                        const int c = c0 + cc;
-                        if (c >= un.rows) break;
                         const float gv = __uint_as_float(gr[cc]);
-                        const float uv = __uint_as_float(ur[cc]);
-                        const float h = gv / (1.0f + expf(-gv)) * uv;
-                        float amax = fabsf(h);
+                        h[cc] = gv / (1.0f + __expf(-gv)) * __uint_as_float(ur[cc]);
+                        am[cc] = fabsf(h[cc]);
+                    }
 #pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-                        const int X = mx_e4m3_exponent(amax);
-                        const uint32_t code = amax > 0.0f ? e4m3_code(h, exp2i(-X)) : 0u;
-                        const int64_t row = un.row0 + c;
-                        g.hq[row * g.I + col] = static_cast<uint8_t>(code);
-                        if (lane == 0) g.hs_t[sf_tile_offset(row, col / 32, kchunks)] = static_cast<uint8_t>(X + 127);
+                    for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc)
+                            am[cc] = fmaxf(am[cc], __shfl_xor_sync(0xFFFFFFFFu, am[cc], off));
+                    }
+                    const int cmax = min(16, un.rows - c0);
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        if (cc < cmax) {
+                            const int X = mx_e4m3_exponent(am[cc]);
+                            const uint32_t code = am[cc] > 0.0f ? e4m3_code(h[cc], exp2i(-X)) : 0u;
+                            const int64_t row = un.row0 + c0 + cc;
+                            g.hq[row * g.I + col] = static_cast<uint8_t>(code);
+                            if (lane == 0)
+                                g.hs_t[act_sf_offset(un.tile, c0 + cc, col / 32, kchunks)] =
+                                    static_cast<uint8_t>(X + 127);
+                        }
                     }
                 }
             } else {
@@ -351,26 +356,26 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
                     const int m = (un.arow[a] - un.expert * g.H) + 32 * q + lane;   // output feature
                     for (int c0 = 0; c0 < un.n; c0 += 16) {
                         uint32_t vr[16];
-                        tmem_ld_32x32b_x16(tmem + lane_base + a * kTile + c0, vr);
+                        tmem_ld_32x32b_x16(acc + a * kTileN + c0, vr);
                         tmem_ld_wait();
+                        const int cmax = min(16, un.rows - c0);
 #pragma unroll
-                        for (int cc = 0; cc < 16; ++cc) {
-                            const int c = c0 + cc;
-                            if (c >= un.rows) break;
-                            g.y[static_cast<int64_t>(un.row0 + c) * g.H + m] = __float2bfloat16_rn(__uint_as_float(vr[cc]));
-                        }
+                        for (int cc = 0; cc < 16; ++cc)
+                            if (cc < cmax)
+                                g.y[static_cast<int64_t>(un.row0 + c0 + cc) * g.H + m] =
+                                    __float2bfloat16_rn(__uint_as_float(vr[cc]));
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(tmem_empty);
+            mbar_arrive(&tmem_empty[buf]);
             if (un.phase == 1) {
                 fence_proxy_async_global();
                 __threadfence();
                 epi_bar_sync();
                 if (threadIdx.x == kEpiWarp0 * 32) atomicAdd(&g.done1[un.tile], 1);
             }
-            acc_phase ^= 1u;
+            ++acc_iter;
         }
     }
 

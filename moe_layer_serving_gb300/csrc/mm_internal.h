@@ -15,9 +15,13 @@ namespace mm {
 
 // ---- tile geometry --------------------------------------------------------
 // Every physical expert's dispatched rows form a segment that starts at a
-// multiple of kTile rows, so one token tile never straddles two experts and
-// its activation scale factors fill whole scale tiles.
-constexpr int kTile = 128;       // token-tile rows, weight rows per MMA (M)
+// multiple of kSegAlign rows; the segment is cut into token tiles of at most
+// kTileN rows, so a tile never straddles two experts.  kTileN = 112 keeps the
+// MMA's N at most 112, which lets two accumulator buffers (2 x 224 fp32
+// columns) and the scale factors (12 columns) share the 512 TMEM columns.
+constexpr int kTile = 128;       // weight rows per MMA (M) and per weight row block
+constexpr int kTileN = 112;      // token rows per tile (MMA N, a multiple of 16)
+constexpr int kSegAlign = 16;    // segment start alignment (rows)
 constexpr int kKStep = 128;      // reduction elements per pipeline stage
 constexpr int kBBox = 16;        // token rows per TMA box of the B operand
 constexpr int kStages = 4;       // shared-memory pipeline depth
@@ -44,9 +48,27 @@ __host__ __device__ inline int64_t sf_tile_offset(int64_t row, int kblock32, int
     return (rb * kchunks + kc) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + (kblock32 % 4);
 }
 
+// Weight tile layout: the packed e2m1 bytes of each (128-row block, 128-wide K
+// block) form one contiguous 8 KB tile, rows of 64 bytes, tiles ordered by row
+// block then K block, so one TMA box is one sequential 8 KB read of HBM.
+__host__ __device__ inline int64_t w_tile_offset(int64_t row, int64_t byte_col, int kblocks)
+{
+    return ((row / 128) * kblocks + byte_col / 64) * 8192 + (row % 128) * 64 + (byte_col % 64);
+}
+
+// Activation scale tiles are per token tile: tile t, row r of the tile
+// (r < 128), 32-element block b along K.
+__host__ __device__ inline int64_t act_sf_offset(int64_t tile, int r, int kblock32, int kchunks)
+{
+    return (tile * kchunks + kblock32 / 4) * 512 + (r % 32) * 16 + (r / 32) * 4 + (kblock32 % 4);
+}
+
+__host__ __device__ inline int seg_rows(int cnt) { return (cnt + kSegAlign - 1) / kSegAlign * kSegAlign; }
+__host__ __device__ inline int tiles_of(int cnt) { return (cnt + kTileN - 1) / kTileN; }
+
 struct GemmMaps {
-    CUtensorMap w1;   // e2m1 [P*2I rows][H]  (16 x 4-bit -> 16-byte smem units)
-    CUtensorMap w2;   // e2m1 [P*H rows][I]
+    CUtensorMap w1;   // e2m1 tiles [P*2I/128 * H/128][128 rows][128]  (16 x 4-bit -> 16-byte smem units)
+    CUtensorMap w2;   // e2m1 tiles [P*H/128 * I/128][128 rows][128]
     CUtensorMap xq;   // e4m3 [rows][H]
     CUtensorMap hq;   // e4m3 [rows][I]
 };
@@ -54,9 +76,9 @@ struct GemmMaps {
 struct GemmArgs {
     const uint8_t* w1_sf;   // tiled [P][2I/128][H/128][512]
     const uint8_t* w2_sf;   // tiled [P][H/128][I/128][512]
-    const uint8_t* xs_t;    // tiled [rows/128][H/128][512]
+    const uint8_t* xs_t;    // per token tile [tiles][H/128][512]
     uint8_t* hq;            // [rows][I]
-    uint8_t* hs_t;          // tiled [rows/128][I/128][512]
+    uint8_t* hs_t;          // per token tile [tiles][I/128][512]
     __nv_bfloat16* y;       // [rows][H]
     const int* tile_expert; // per token tile
     const int* tile_row0;
@@ -90,12 +112,13 @@ struct mm_ctx {
     size_t ws_bytes = 0;
     int32_t *idx = nullptr, *phys = nullptr, *pos = nullptr;
     float* wgt = nullptr;
-    int32_t *chunk_hist = nullptr, *off = nullptr, *tile_expert = nullptr, *tile_row0 = nullptr,
+    int32_t *chunk_hist = nullptr, *off = nullptr, *toff = nullptr, *tile_expert = nullptr, *tile_row0 = nullptr,
             *tile_rows = nullptr, *num_tiles = nullptr, *done1 = nullptr;
     uint8_t *xq = nullptr, *xs_t = nullptr, *hq = nullptr, *hs_t = nullptr;
     __nv_bfloat16* y = nullptr;
     int* status = nullptr;
     unsigned* grid_bar = nullptr;   // fused kernel's grid barrier {count, generation}
+    uint64_t* stamps = nullptr;     // fused kernel's per-CTA stage timestamps [sms][8]
     mm::GemmMaps maps{};
     bool maps_weights = false, maps_ws = false;
     // per-launch timing of the dominant kernel: event pairs, pairs recorded so far
@@ -126,6 +149,7 @@ cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s);
 cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s);
 cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s);
+cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s);
 cudaError_t gemm_prepare(int dev);
 cudaError_t small_prepare();
 cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logits, const float* bias, void* out,

@@ -8,7 +8,7 @@
 // the library instead of caller- or library-allocated workspace.
 //
 // It is a single-CTA variant of the permute kernels (chunk histograms ->
-// per-expert scan into 128-row-aligned segments -> stable scatter), producing
+// per-expert scan into aligned segments -> stable scatter), producing
 // the same dispatch rows and segment offsets as mm_forward's permute.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -56,12 +56,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
         cnt[p] = run;
     }
     __syncthreads();
-    // 4. segment starts, each segment padded to a multiple of the token tile
+    // 4. segment starts, each segment padded to the forward's segment alignment
     if (threadIdx.x == 0) {
         int o = 0;
         for (int p = 0; p < P; ++p) {
             soff[p] = o;
-            o += (cnt[p] + mm::kTile - 1) / mm::kTile * mm::kTile;
+            o += mm::seg_rows(cnt[p]);
         }
         soff[P] = o;
     }

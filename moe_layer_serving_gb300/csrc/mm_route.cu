@@ -1,6 +1,6 @@
 // mm_route.cu -- the SIMT stages of the fused MoE forward on sm_103a:
 //   router (sigmoid top-k) + fused EPLB remap + per-expert load recording,
-//   the stable permute into expert-sorted 128-row segments,
+//   the stable permute into expert-sorted segments (16-row aligned),
 //   MXFP8 activation quantisation fused with the dispatch copy,
 //   the deterministic gather combine,
 //   and the re-layout of e8m0 scales into scale tiles (weights, at load time).
@@ -35,8 +35,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// permute: chunk histograms -> per-expert scan (segments padded to 128 rows,
-// token-tile table) -> stable scatter (pairs keep (token, slot) order)
+// permute: chunk histograms -> per-expert scan (segments padded to 16 rows,
+// token tiles of up to 112 rows) -> stable scatter (pairs keep (token, slot) order)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) hist_kernel(const int32_t* phys, int64_t npairs, int P, int32_t* chunk_hist)
 {
@@ -82,6 +82,7 @@ struct ScanArgs {
     int32_t* chunk_hist;   // in: counts per chunk; out: exclusive base per chunk
     int nchunks, P;
     int32_t* off;          // [P+1] padded segment starts
+    int32_t* toff;         // [P] first token tile of each expert
     int32_t* tile_expert;
     int32_t* tile_row0;
     int32_t* tile_rows;
@@ -102,18 +103,19 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
             cnt += v;
         }
     }
-    const int padded = (cnt + kTile - 1) / kTile * kTile;
-    const int tiles = padded / kTile;
+    const int padded = seg_rows(cnt);
+    const int tiles = tiles_of(cnt);
     const int off_incl = block_scan_incl(padded, warp_tot);
     const int tiles_incl = block_scan_incl(tiles, warp_tot);
     if (p < a.P) {
         const int off = off_incl - padded;
         const int t0 = tiles_incl - tiles;
         a.off[p] = off;
+        a.toff[p] = t0;
         for (int t = 0; t < tiles; ++t) {
             a.tile_expert[t0 + t] = p;
-            a.tile_row0[t0 + t] = off + t * kTile;
-            a.tile_rows[t0 + t] = min(kTile, cnt - t * kTile);
+            a.tile_row0[t0 + t] = off + t * kTileN;
+            a.tile_rows[t0 + t] = min(kTileN, cnt - t * kTileN);
             a.done1[t0 + t] = 0;
         }
         if (p == a.P - 1) {
@@ -157,13 +159,16 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* phys, int64_
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(const __nv_bfloat16* __restrict__ x, int64_t T, int H,
                                                             int k, const int32_t* __restrict__ pos,
+                                                            const int32_t* __restrict__ phys,
+                                                            const int32_t* __restrict__ off,
+                                                            const int32_t* __restrict__ toff,
                                                             uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t)
 {
     const int nb = H / 32;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = g / nb;
     if (t >= T) return;
-    quant_dispatch_block(x, t, static_cast<int>(g % nb), H, k, pos + t * k, xq, xs_t);
+    quant_dispatch_block(x, t, static_cast<int>(g % nb), H, k, pos + t * k, phys + t * k, off, toff, xq, xs_t);
 }
 
 // ---------------------------------------------------------------------------
@@ -189,6 +194,17 @@ __global__ void tile_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __r
     const int64_t r = g / nb;
     const int b = static_cast<int>(g % nb);
     dst[sf_tile_offset(r, b, K / 128)] = src[g];
+}
+
+// packed e2m1 [rows][K/2] -> 8 KB weight tiles, 16 bytes per thread
+__global__ void tile_weights_kernel(const uint4* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K)
+{
+    const int per_row = K / 32;                    // 16-byte pieces per row
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (g >= rows * per_row) return;
+    const int64_t r = g / per_row;
+    const int c = static_cast<int>(g % per_row) * 16;
+    *reinterpret_cast<uint4*>(dst + w_tile_offset(r, c, K / 128)) = src[g];
 }
 
 unsigned grid_for(int64_t threads, int block) { return static_cast<unsigned>((threads + block - 1) / block); }
@@ -224,6 +240,7 @@ cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
     a.nchunks = nchunks;
     a.P = c->P;
     a.off = c->off;
+    a.toff = c->toff;
     a.tile_expert = c->tile_expert;
     a.tile_row0 = c->tile_row0;
     a.tile_rows = c->tile_rows;
@@ -238,7 +255,8 @@ cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T
 {
     const int64_t threads = T * (c->H / 32);
     quant_dispatch_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hidden), T, c->H,
-                                                                 c->k, c->pos, c->xq, c->xs_t);
+                                                                 c->k, c->pos, c->phys, c->off, c->toff, c->xq,
+                                                                 c->xs_t);
     return cudaGetLastError();
 }
 
@@ -247,6 +265,13 @@ cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s
     const int64_t threads = T * (c->H / 8);
     combine_kernel<<<grid_for(threads, 256), 256, 0, s>>>(c->y, c->wgt, c->pos, T, c->H, c->k,
                                                           static_cast<__nv_bfloat16*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s)
+{
+    const int64_t threads = rows * (K / 32);
+    tile_weights_kernel<<<grid_for(threads, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), dst, rows, K);
     return cudaGetLastError();
 }
 

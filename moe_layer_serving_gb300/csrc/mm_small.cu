@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kSmallWarps = kThreads / 32;
 constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
-constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kTile;
+constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kTileN + 1;
 constexpr int kSmallSmemBytes = kGemmSmemBytes + 3 * kMaxSmallTiles * 4 + 64 + 1024;
 
 struct SmallArgs {
@@ -46,6 +46,7 @@ struct SmallArgs {
     uint8_t* xq;              // dispatched activation codes [rows, H]
     uint8_t* xs_t;            // their scale tiles
     unsigned* bar;            // grid barrier {count, generation}
+    uint64_t* stamps;         // [gridDim.x][8] %globaltimer at the stage boundaries
     int P;
 };
 
@@ -101,13 +102,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t T = a.route.T;
     const int k = a.route.k, P = a.P, H = g.H;
     const int N = static_cast<int>(T) * k;
+    uint64_t* stamp = a.stamps + static_cast<int64_t>(blockIdx.x) * 8;
+    if (threadIdx.x == 0) stamp[0] = globaltimer();
 
     // ---- A: route + EPLB remap + record ----------------------------------
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * kSmallWarps + warp; t < T;
          t += static_cast<int64_t>(gridDim.x) * kSmallWarps)
         route_token_any(a.route, t, lane, nullptr);
 
+    if (threadIdx.x == 0) stamp[1] = globaltimer();
     bool ok = grid_sync(a.bar, g.status, s.abort_flag);
+    if (threadIdx.x == 0) stamp[2] = globaltimer();
 
     // ---- C: permute, redundantly per CTA, in the (idle) pipeline buffers ----
     int* sphys = reinterpret_cast<int*>(s.stages);          // [N]
@@ -148,8 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p0 = lane * per, p1 = min(P, p0 + per);
             int rows = 0, tiles = 0;
             for (int p = p0; p < p1; ++p) {
-                rows += (cnt[p] + kTile - 1) / kTile * kTile;
-                tiles += (cnt[p] + kTile - 1) / kTile;
+                rows += seg_rows(cnt[p]);
+                tiles += tiles_of(cnt[p]);
             }
             int rx = rows, tx = tiles;
 #pragma unroll
@@ -165,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = p0; p < p1; ++p) {
                 soff[p] = ro;
                 stoff[p] = to;
-                ro += (cnt[p] + kTile - 1) / kTile * kTile;
-                to += (cnt[p] + kTile - 1) / kTile;
+                ro += seg_rows(cnt[p]);
+                to += tiles_of(cnt[p]);
             }
             if (lane == 31) {
                 soff[P] = rx;
@@ -176,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         for (int p = threadIdx.x; p < P; p += kThreads) {
-            const int nt = (cnt[p] + kTile - 1) / kTile;
+            const int nt = tiles_of(cnt[p]);
             for (int t = 0; t < nt; ++t) {
                 t_expert[stoff[p] + t] = p;
-                t_row0[stoff[p] + t] = soff[p] + t * kTile;
-                t_rows[stoff[p] + t] = min(kTile, cnt[p] - t * kTile);
+                t_row0[stoff[p] + t] = soff[p] + t * kTileN;
+                t_rows[stoff[p] + t] = min(kTileN, cnt[p] - t * kTileN);
             }
         }
         for (int base = lo; base < hi; base += 32) {
@@ -214,12 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < T * nb;
              it += static_cast<int64_t>(gridDim.x) * kThreads) {
             const int64_t t = it / nb;
-            quant_dispatch_block(a.x, t, static_cast<int>(it % nb), H, k, spos + t * k, a.xq, a.xs_t);
+            quant_dispatch_block(a.x, t, static_cast<int>(it % nb), H, k, spos + t * k, sphys + t * k, soff, stoff,
+                                 a.xq, a.xs_t);
         }
         fence_proxy_async_global();
     }
     fence_proxy_async_shared();     // scratch writes above precede the TMA writes into the same buffers
+    if (threadIdx.x == 0) stamp[3] = globaltimer();
     ok = grid_sync(a.bar, g.status, s.abort_flag);
+    if (threadIdx.x == 0) stamp[4] = globaltimer();
 
     // ---- F: GEMM1 + SwiGLU + requant, GEMM2 (tiles from shared memory) -----
     if (ok) {
@@ -231,7 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         gemm_roles(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
     }
     gemm_teardown(tmem);
+    if (threadIdx.x == 0) stamp[5] = globaltimer();
     ok = grid_sync(a.bar, g.status, s.abort_flag);
+    if (threadIdx.x == 0) stamp[6] = globaltimer();
 
     // ---- H: combine ---------------------------------------------------------
     if (ok) {
@@ -240,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
              it += static_cast<int64_t>(gridDim.x) * kThreads)
             combine_chunk(g.y, a.route.w, a.pos, it / nc, static_cast<int>(it % nc), H, k, a.out);
     }
+    __syncthreads();
+    if (threadIdx.x == 0) stamp[7] = globaltimer();
 }
 
 }  // namespace
@@ -281,6 +293,7 @@ cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logit
     a.xq = c->xq;
     a.xs_t = c->xs_t;
     a.bar = c->grid_bar;
+    a.stamps = c->stamps;
     a.P = c->P;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c->sms));

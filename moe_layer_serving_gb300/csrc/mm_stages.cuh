@@ -141,10 +141,14 @@ __device__ __forceinline__ void route_token_any(const RouteArgs& a, int64_t t, i
 
 // MXFP8 quantisation of block b (32 elements) of token t and its dispatch to
 // the token's k rows: 4 x 128-bit loads, one e8m0 scale, 32 e4m3 codes per
-// row (2 x 128-bit stores).  pos_t points at the k dispatch rows of token t.
+// row (2 x 128-bit stores).  pos_t / phys_t: the k dispatch rows and physical
+// experts of token t; off / toff: segment start row and first token tile of
+// each expert (global or shared memory), which place the scale byte in the
+// scale tile of the row's token tile.
 __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
-                                                     int k, const int32_t* pos_t, uint8_t* __restrict__ xq,
-                                                     uint8_t* __restrict__ xs_t)
+                                                     int k, const int32_t* pos_t, const int32_t* phys_t,
+                                                     const int32_t* off, const int32_t* toff,
+                                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t)
 {
     const uint4* src = reinterpret_cast<const uint4*>(x + t * H + b * 32);
     float v[32];
@@ -180,7 +184,9 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
         uint4* dst = reinterpret_cast<uint4*>(xq + row * H + b * 32);
         dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        xs_t[sf_tile_offset(row, b, kchunks)] = sbyte;
+        const int p = phys_t[j];
+        const int rank = static_cast<int>(row) - off[p];
+        xs_t[act_sf_offset(toff[p] + rank / kTileN, rank % kTileN, b, kchunks)] = sbyte;
     }
 }
 

@@ -128,7 +128,7 @@ def check_against_oracle(cfg, res, hidden, logits, bias, W, map_rc, token_sel=No
     assert np.array_equal(res["phys"], phys), "physical experts differ"
     off_o, order, pos_o = oracle.permute(phys, P)
     cnt = np.diff(off_o)
-    padded = (cnt + 127) // 128 * 128
+    padded = (cnt + 15) // 16 * 16
     off_g = np.concatenate([[0], np.cumsum(padded)])
     assert np.array_equal(res["offsets"], off_g), "segment offsets differ"
     p_flat = phys.ravel()
