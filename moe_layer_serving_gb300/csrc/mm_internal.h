@@ -19,19 +19,27 @@ namespace mm {
 // kTileN rows, so a tile never straddles two experts.  kTileN = 112 keeps the
 // MMA's N at most 112, which lets two accumulator buffers (2 x 224 fp32
 // columns) and the scale factors (12 columns) share the 512 TMEM columns.
+// Build-time tuning knobs (defaults are the shipped configuration).
+#ifndef MM_TILE_N
+#define MM_TILE_N 112
+#endif
+#ifndef MM_STAGES
+#define MM_STAGES 4
+#endif
 constexpr int kTile = 128;       // weight rows per MMA (M) and per weight row block
-constexpr int kTileN = 112;      // token rows per tile (MMA N, a multiple of 16)
+constexpr int kTileN = MM_TILE_N;  // token rows per tile (MMA N, a multiple of 16, <= 112)
 constexpr int kSegAlign = 16;    // segment start alignment (rows)
 constexpr int kKStep = 128;      // reduction elements per pipeline stage
 constexpr int kBBox = 16;        // token rows per TMA box of the B operand
-constexpr int kStages = 4;       // shared-memory pipeline depth
+constexpr int kStages = MM_STAGES;  // shared-memory pipeline depth
+static_assert(kTileN % 16 == 0 && kTileN <= 112, "token tile must be a multiple of 16, at most 112 rows");
 constexpr int kChunkPairs = 1024;  // (token, slot) pairs per permute chunk
 constexpr int kSmallMaxTokens = 512;  // largest batch the fused small-input kernel takes
 
 // shared-memory stage: A0 | A1 | B | SF(A0, A1, B)
 constexpr int kATileBytes = kTile * kKStep;          // e2m1 unpacked to 1 byte/element in smem
 constexpr int kATileTxBytes = kTile * kKStep / 2;    // what the TMA counts: the packed global bytes
-constexpr int kBTileBytes = kTile * kKStep;          // e4m3, up to 128 token rows
+constexpr int kBTileBytes = ((kTileN * kKStep + 1023) / 1024) * 1024;  // e4m3 token rows of one tile
 constexpr int kSFBytes = 512;                        // 128 rows x 4 scale bytes
 constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes + 4 * kSFBytes;
 

@@ -84,8 +84,9 @@ __device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int l
             avail |= 1u << i;
         }
     }
-    int sel_e[MM_MAX_TOPK];
-    float sel_s[MM_MAX_TOPK];
+    // lane j keeps the j-th selection
+    int my_e = 0;
+    float my_s = 0.0f;
 #pragma unroll
     for (int j = 0; j < MM_MAX_TOPK; ++j) {
         if (j >= a.k) break;
@@ -111,22 +112,23 @@ __device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int l
             }
         }
         if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
-        sel_e[j] = be;
-        sel_s[j] = bs;
+        if (lane == j) {
+            my_e = be;
+            my_s = bs;
+        }
     }
-    if (lane == 0) {
-        float S = sel_s[0];
-        for (int j = 1; j < a.k; ++j) S = __fadd_rn(S, sel_s[j]);
-        for (int j = 0; j < a.k; ++j) {
-            const int e = sel_e[j];
-            const int slot = static_cast<int>((t + j) % a.rc[e]);
-            a.idx[t * a.k + j] = e;
-            a.w[t * a.k + j] = __fdiv_rn(sel_s[j], S);
-            a.phys[t * a.k + j] = a.map[static_cast<int64_t>(e) * a.R + slot];
-            if (a.counts) {
-                if (hist) atomicAdd(&hist[e], 1);
-                else atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + e), 1ull);
-            }
+    // sum of the selected scores in selection order (the same in every lane)
+    float S = __shfl_sync(0xFFFFFFFFu, my_s, 0);
+    for (int j = 1; j < a.k; ++j) S = __fadd_rn(S, __shfl_sync(0xFFFFFFFFu, my_s, j));
+    if (lane < a.k) {
+        const int e = my_e;
+        const uint32_t slot = static_cast<uint32_t>(t + lane) % static_cast<uint32_t>(a.rc[e]);
+        a.idx[t * a.k + lane] = e;
+        a.w[t * a.k + lane] = __fdiv_rn(my_s, S);
+        a.phys[t * a.k + lane] = a.map[e * a.R + static_cast<int>(slot)];
+        if (a.counts) {
+            if (hist) atomicAdd(&hist[e], 1);
+            else atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + e), 1ull);
         }
     }
 }
