@@ -296,7 +296,7 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     // each non-empty segment adds < kSegAlign pad rows and < 1 partial token tile
     const int64_t busy = npairs < c->P ? npairs : c->P;
     const int64_t rows = npairs + busy * (mm::kSegAlign - 1) + mm::kSegAlign;
-    const int64_t tiles = npairs / mm::kTileN + busy + 1;
+    const int64_t tiles = npairs / mm::kTokTile + busy + 1;
     const int64_t chunks = (npairs + mm::kChunkPairs - 1) / mm::kChunkPairs;
     const int64_t H = c->H, I = c->I;
     // size pass, then carve

@@ -244,14 +244,15 @@ __device__ __forceinline__ uint64_t desc_sf(const void* sf)
     return smem_desc(smem_u32(sf), 0, 128, kSwizzleNone);
 }
 
-// Instruction descriptor, block-scaled kinds: A = e2m1 (format 5), B = e4m3
-// (format 0), e8m0 scales, both K-major, M = 128, N = n (multiple of 16).
-__device__ __forceinline__ uint32_t idesc_e2m1_e4m3(uint32_t n, uint32_t sf_id)
+// Instruction descriptor, block-scaled kinds: A = e4m3 (format 0), B = e2m1
+// (format 5), e8m0 scales, both K-major, M = 128, N = n (multiple of 16, <= 256);
+// sf_id picks the scale byte (the 32-wide K block) inside each scale column.
+__device__ __forceinline__ uint32_t idesc_e4m3_e2m1(uint32_t n, uint32_t sf_id)
 {
     uint32_t d = 0;
     d |= (sf_id & 3u) << 4;       // B scale-factor byte
-    d |= 5u << 7;                 // A format: e2m1
-    d |= 0u << 10;                // B format: e4m3
+    d |= 0u << 7;                 // A format: e4m3
+    d |= 5u << 10;                // B format: e2m1
     d |= (n >> 3) << 17;          // N / 8
     d |= 1u << 23;                // scale format: ue8m0
     d |= (128u >> 4) << 24;       // M / 16

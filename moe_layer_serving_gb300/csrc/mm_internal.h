@@ -14,34 +14,32 @@
 namespace mm {
 
 // ---- tile geometry --------------------------------------------------------
+// Both GEMMs put one token tile on the MMA's M side (128 rows, e4m3) and 256
+// weight rows on its N side (e2m1), K in stages of 128.  A block-scaled
+// tcgen05 MMA costs about the same time whatever its N, so every instruction
+// is issued at the full N = 256 (gate + up rows of 128 I-columns for GEMM1,
+// 256 output features for GEMM2).
 // Every physical expert's dispatched rows form a segment that starts at a
-// multiple of kSegAlign rows; the segment is cut into token tiles of at most
-// kTileN rows, so a tile never straddles two experts.  kTileN = 112 keeps the
-// MMA's N at most 112, which lets two accumulator buffers (2 x 224 fp32
-// columns) and the scale factors (12 columns) share the 512 TMEM columns.
-// Build-time tuning knobs (defaults are the shipped configuration).
-#ifndef MM_TILE_N
-#define MM_TILE_N 112
-#endif
+// multiple of kSegAlign rows and is cut into token tiles of kTokTile rows, so
+// a tile never straddles two experts.
 #ifndef MM_STAGES
 #define MM_STAGES 4
 #endif
-constexpr int kTile = 128;       // weight rows per MMA (M) and per weight row block
-constexpr int kTileN = MM_TILE_N;  // token rows per tile (MMA N, a multiple of 16, <= 112)
+constexpr int kTile = 128;       // weight rows per TMA box / weight row block
+constexpr int kTokTile = 128;    // token rows per tile (the MMA's M)
 constexpr int kSegAlign = 16;    // segment start alignment (rows)
 constexpr int kKStep = 128;      // reduction elements per pipeline stage
-constexpr int kBBox = 16;        // token rows per TMA box of the B operand
+constexpr int kBBox = 16;        // token rows per TMA box of the token operand
 constexpr int kStages = MM_STAGES;  // shared-memory pipeline depth
-static_assert(kTileN % 16 == 0 && kTileN <= 112, "token tile must be a multiple of 16, at most 112 rows");
 constexpr int kChunkPairs = 1024;  // (token, slot) pairs per permute chunk
 constexpr int kSmallMaxTokens = 512;  // largest batch the fused small-input kernel takes
 
-// shared-memory stage: A0 | A1 | B | SF(A0, A1, B)
-constexpr int kATileBytes = kTile * kKStep;          // e2m1 unpacked to 1 byte/element in smem
-constexpr int kATileTxBytes = kTile * kKStep / 2;    // what the TMA counts: the packed global bytes
-constexpr int kBTileBytes = ((kTileN * kKStep + 1023) / 1024) * 1024;  // e4m3 token rows of one tile
+// shared-memory stage: tokens (A) | weights (B, two 128-row boxes) | SF(A, B0, B1)
+constexpr int kABytes = kTokTile * kKStep;           // e4m3 token rows
+constexpr int kWBoxBytes = kTile * kKStep;           // e2m1 unpacked to 1 byte/element in smem
+constexpr int kWBoxTxBytes = kTile * kKStep / 2;     // what the TMA counts: the packed global bytes
 constexpr int kSFBytes = 512;                        // 128 rows x 4 scale bytes
-constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes + 4 * kSFBytes;
+constexpr int kStageBytes = kABytes + 2 * kWBoxBytes + 4 * kSFBytes;
 
 // Scale-factor tile layout, shared by weights and activations.  Rows are
 // grouped by 128 and K by 128 (4 scale bytes per row); each group is one
@@ -72,7 +70,7 @@ __host__ __device__ inline int64_t act_sf_offset(int64_t tile, int r, int kblock
 }
 
 __host__ __device__ inline int seg_rows(int cnt) { return (cnt + kSegAlign - 1) / kSegAlign * kSegAlign; }
-__host__ __device__ inline int tiles_of(int cnt) { return (cnt + kTileN - 1) / kTileN; }
+__host__ __device__ inline int tiles_of(int cnt) { return (cnt + kTokTile - 1) / kTokTile; }
 
 struct GemmMaps {
     CUtensorMap w1;   // e2m1 tiles [P*2I/128 * H/128][128 rows][128]  (16 x 4-bit -> 16-byte smem units)

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a)
 
 // ---------------------------------------------------------------------------
 // permute: chunk histograms -> per-expert scan (segments padded to 16 rows,
-// token tiles of up to 112 rows) -> stable scatter (pairs keep (token, slot) order)
+// token tiles of up to 128 rows) -> stable scatter (pairs keep (token, slot) order)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) hist_kernel(const int32_t* phys, int64_t npairs, int P, int32_t* chunk_hist)
 {
@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
         a.toff[p] = t0;
         for (int t = 0; t < tiles; ++t) {
             a.tile_expert[t0 + t] = p;
-            a.tile_row0[t0 + t] = off + t * kTileN;
-            a.tile_rows[t0 + t] = min(kTileN, cnt - t * kTileN);
+            a.tile_row0[t0 + t] = off + t * kTokTile;
+            a.tile_rows[t0 + t] = min(kTokTile, cnt - t * kTokTile);
             a.done1[t0 + t] = 0;
         }
         if (p == a.P - 1) {

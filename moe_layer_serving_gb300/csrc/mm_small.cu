@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kSmallWarps = kThreads / 32;
 constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
-constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kTileN + 1;
+constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kTokTile + 1;
 constexpr int kSmallSmemBytes = kGemmSmemBytes + 3 * kMaxSmallTiles * 4 + 64 + 1024;
 
 struct SmallArgs {
@@ -184,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = tiles_of(cnt[p]);
             for (int t = 0; t < nt; ++t) {
                 t_expert[stoff[p] + t] = p;
-                t_row0[stoff[p] + t] = soff[p] + t * kTileN;
-                t_rows[stoff[p] + t] = min(kTileN, cnt[p] - t * kTileN);
+                t_row0[stoff[p] + t] = soff[p] + t * kTokTile;
+                t_rows[stoff[p] + t] = min(kTokTile, cnt[p] - t * kTokTile);
             }
         }
         for (int base = lo; base < hi; base += 32) {

@@ -188,7 +188,7 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         const int p = phys_t[j];
         const int rank = static_cast<int>(row) - off[p];
-        xs_t[act_sf_offset(toff[p] + rank / kTileN, rank % kTileN, b, kchunks)] = sbyte;
+        xs_t[act_sf_offset(toff[p] + rank / kTokTile, rank % kTokTile, b, kchunks)] = sbyte;
     }
 }
 
