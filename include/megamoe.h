@@ -183,6 +183,27 @@ MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t by
 /* Size in bytes of a debug stage for the last forward (0 before any). */
 MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);
 
+/* EPLB replica planner (host only, no CUDA).  load [E] (host): recorded
+ * tokens per logical expert, e.g. from mm_read_counts over a rebalance
+ * interval (the pages rebalance every 200 iterations from the recorder's
+ * statistics, "sglang PR #35619", EPLB arm settings).  Every logical expert e
+ * keeps physical slot e; each redundant slot E..P-1 in turn goes to the
+ * expert with the highest load per replica (load[e] / replicas, compared
+ * exactly; the lower index on ties) among those below max_replicas.  Writes
+ * phys_of_logical [E, max_replicas] (unused entries -1) and replica_counts
+ * [E], ready for mm_set_eplb_map.  MM_ERR_INVALID_ARG if P - E slots cannot be
+ * placed under max_replicas. */
+MM_API mm_status mm_plan_replicas(const int64_t *load, int num_experts, int num_physical, int max_replicas,
+                                  int32_t *phys_of_logical, int32_t *replica_counts);
+
+/* Rebalance the handle's replicas from the counts recorded in slot `layer`:
+ * plans with mm_plan_replicas, copies each re-assigned physical slot's
+ * weights on the device from its logical expert's own slot (slot e must hold
+ * logical e), and installs the new map.  Synchronous; not allowed during
+ * stream capture.  A no-op when P == E.  Outputs of later forwards are
+ * unchanged (replicas are byte copies); only the load spread changes. */
+MM_API mm_status mm_rebalance(mm_handle h, int layer, int max_replicas);
+
 /* Per-launch timing of the dominant kernel (the grouped GEMM, or the fused
  * small-input kernel).  mm_profile_begin creates max_launches pairs of CUDA
  * events (allocation: call it outside stream capture); each later mm_forward

@@ -49,6 +49,8 @@ _SIGS = {
     "mm_profile_begin": [_p, _i32],
     "mm_profile_end": [_p, _p, _i32, C.POINTER(_i32)],
     "mm_plan_dispatch_static": [_p, _i64, _i32, _p, _p, _p],
+    "mm_plan_replicas": [_p, _i32, _i32, _i32, _p, _p],
+    "mm_rebalance": [_p, _i32, _i32],
 }
 _lib = None
 
@@ -82,6 +84,17 @@ def _export(name):
 for _n in list(_SIGS) + ["mm_status_string"]:
     globals()[_n] = _export(_n)
     __all__.append(_n)
+
+
+def plan_replicas(load, num_physical: int, max_replicas: int):
+    """Host replica planner -> (phys_of_logical int32 [E, R], replica_counts int32 [E])."""
+    load = np.ascontiguousarray(load, np.int64)
+    E = load.size
+    pol = np.zeros((E, max_replicas), np.int32)
+    rc = np.zeros(E, np.int32)
+    _check(lib().mm_plan_replicas(load.ctypes.data, E, num_physical, max_replicas, pol.ctypes.data, rc.ctypes.data),
+           "mm_plan_replicas")
+    return pol, rc
 
 
 class MegaMoEError(RuntimeError):
@@ -147,6 +160,10 @@ class MegaMoE:
         m = np.ascontiguousarray(phys_of_logical, np.int32)
         rc = np.ascontiguousarray(replica_counts, np.int32)
         _check(lib().mm_set_eplb_map(self._h, m.ctypes.data, rc.ctypes.data, m.shape[1]), "mm_set_eplb_map")
+
+    def rebalance(self, layer: int, max_replicas: int) -> None:
+        """Re-plan the replicas from the counts of `layer` and install them."""
+        _check(lib().mm_rebalance(self._h, layer, max_replicas), "mm_rebalance")
 
     def bind_layer(self, layer: int) -> None:
         _check(lib().mm_bind_layer(self._h, layer), "mm_bind_layer")

@@ -48,14 +48,15 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t cols,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Weight tiles [nblocks][128 rows][128 e2m1], one 8 KB box per (row block, K block).
-bool make_weight_map(CUtensorMap* m, void* base, uint64_t nblocks)
+// Weight blocks [nblocks][128 rows][128 e2m1]; a box is `depth` consecutive
+// blocks (a GEMM unit's pair, or one block).
+bool make_weight_map(CUtensorMap* m, void* base, uint64_t nblocks, uint32_t depth)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {128, 128, nblocks};
     const cuuint64_t strides[2] = {64, 8192};
-    const cuuint32_t box[3] = {128, 128, 1};
+    const cuuint32_t box[3] = {128, 128, depth};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -202,8 +203,10 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
     if (!aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1s, 16) || !aligned(w2s, 16)) return MM_ERR_INVALID_ARG;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
     const size_t P = c->P, H = c->H, I = c->I;
-    const size_t n_w1 = P * 2 * I * H / 2, n_w1s = P * 2 * I * H / 32;
-    const size_t n_w2 = P * H * I / 2, n_w2s = P * H * I / 32;
+    const mm::WOrder o1 = mm::w1_order(c->H, c->I), o2 = mm::w2_order(c->H, c->I);
+    const size_t b1 = mm::w_blocks(o1, c->P), b2 = mm::w_blocks(o2, c->P);
+    const size_t n_w1 = b1 * 8192, n_w1s = b1 * 512;
+    const size_t n_w2 = b2 * 8192, n_w2s = b2 * 512;
     if (!c->w1) {
         if (cudaMalloc(&c->w1, n_w1) != cudaSuccess || cudaMalloc(&c->w1_sf, n_w1s) != cudaSuccess ||
             cudaMalloc(&c->w2, n_w2) != cudaSuccess || cudaMalloc(&c->w2_sf, n_w2s) != cudaSuccess) {
@@ -211,13 +214,14 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
             return MM_ERR_CUDA;
         }
     }
-    CK(mm::launch_tile_weights(w1, c->w1, static_cast<int64_t>(P * 2 * I), c->H, nullptr));
-    CK(mm::launch_tile_weights(w2, c->w2, static_cast<int64_t>(P * H), c->I, nullptr));
-    CK(mm::launch_tile_scales(w1s, c->w1_sf, static_cast<int64_t>(P * 2 * I), c->H, nullptr));
-    CK(mm::launch_tile_scales(w2s, c->w2_sf, static_cast<int64_t>(P * H), c->I, nullptr));
+    if (n_w2 != P * H * I / 2) CK(cudaMemset(c->w2, 0, n_w2));       // absent halves of a ragged last group
+    CK(mm::launch_tile_weights(w1, c->w1, static_cast<int64_t>(P * 2 * I), c->H, o1, nullptr));
+    CK(mm::launch_tile_weights(w2, c->w2, static_cast<int64_t>(P * H), c->I, o2, nullptr));
+    CK(mm::launch_tile_scales(w1s, c->w1_sf, static_cast<int64_t>(P * 2 * I), c->H, o1, nullptr));
+    CK(mm::launch_tile_scales(w2s, c->w2_sf, static_cast<int64_t>(P * H), c->I, o2, nullptr));
     CK(cudaDeviceSynchronize());
-    if (!make_weight_map(&c->maps.w1, c->w1, (P * 2 * I / kTile) * (H / 128)) ||
-        !make_weight_map(&c->maps.w2, c->w2, (P * H / kTile) * (I / 128)))
+    if (!make_weight_map(&c->maps.w1, c->w1, b1, 2) || !make_weight_map(&c->maps.w2, c->w2, b2, 2) ||
+        !make_weight_map(&c->maps.w2_one, c->w2, b2, 1))
         return MM_ERR_CUDA;
     c->maps_weights = true;
     c->weights_set = true;
@@ -262,8 +266,76 @@ mm_status mm_set_eplb_map(mm_handle c, const int32_t* pol, const int32_t* rc, in
     c->map = dm;
     c->rc = drc;
     c->R = R;
+    c->host_map = m;
+    c->host_rc.assign(rc, rc + c->E);
     c->map_set = true;
     return MM_OK;
+}
+
+mm_status mm_plan_replicas(const int64_t* load, int E, int P, int max_replicas, int32_t* pol, int32_t* rc)
+{
+    if (!load || !pol || !rc || E < 1 || P < E || P > MM_MAX_EXPERTS || max_replicas < 1) return MM_ERR_INVALID_ARG;
+    if (P - E > static_cast<int64_t>(E) * (max_replicas - 1)) return MM_ERR_INVALID_ARG;
+    for (int e = 0; e < E; ++e)
+        if (load[e] < 0) return MM_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < static_cast<int64_t>(E) * max_replicas; ++i) pol[i] = -1;
+    for (int e = 0; e < E; ++e) {
+        pol[static_cast<int64_t>(e) * max_replicas] = e;       // every expert keeps its own slot
+        rc[e] = 1;
+    }
+    for (int slot = E; slot < P; ++slot) {
+        // the expert with the highest load per replica (exact: cross-multiplied), lower index on ties
+        int best = -1;
+        for (int e = 0; e < E; ++e) {
+            if (rc[e] >= max_replicas) continue;
+            if (best < 0) {
+                best = e;
+                continue;
+            }
+            const __int128 lhs = static_cast<__int128>(load[e]) * rc[best];
+            const __int128 rhs = static_cast<__int128>(load[best]) * rc[e];
+            if (lhs > rhs) best = e;
+        }
+        pol[static_cast<int64_t>(best) * max_replicas + rc[best]] = slot;
+        rc[best] += 1;
+    }
+    return MM_OK;
+}
+
+mm_status mm_rebalance(mm_handle c, int layer, int max_replicas)
+{
+    if (!c || layer < 0 || layer >= MM_MAX_LAYERS || max_replicas < 1) return MM_ERR_INVALID_ARG;
+    if (!c->weights_set || !c->map_set) return MM_ERR_NOT_READY;
+    if (c->P == c->E) return MM_OK;
+    if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    std::vector<int64_t> load(c->E);
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(load.data(), c->counts + static_cast<int64_t>(layer) * c->E, sizeof(int64_t) * c->E,
+                  cudaMemcpyDeviceToHost));
+    std::vector<int32_t> pol(static_cast<size_t>(c->E) * max_replicas), rc(c->E);
+    mm_status st = mm_plan_replicas(load.data(), c->E, c->P, max_replicas, pol.data(), rc.data());
+    if (st != MM_OK) return st;
+    // which logical expert each physical slot holds now, and will hold
+    std::vector<int> now(c->P, -1), next(c->P, -1);
+    for (int e = 0; e < c->E; ++e) {
+        for (int r = 0; r < c->host_rc[e]; ++r) now[c->host_map[static_cast<size_t>(e) * c->R + r]] = e;
+        for (int r = 0; r < rc[e]; ++r) next[pol[static_cast<size_t>(e) * max_replicas + r]] = e;
+    }
+    for (int e = 0; e < c->E; ++e)
+        if (now[e] != e) return MM_ERR_NOT_READY;              // slot e must hold logical e (the copy source)
+    // copy the weights of every slot whose logical expert changes from that expert's own slot
+    const mm::WOrder o1 = mm::w1_order(c->H, c->I), o2 = mm::w2_order(c->H, c->I);
+    const size_t e1 = mm::w_blocks(o1, 1), e2 = mm::w_blocks(o2, 1);   // blocks per expert
+    for (int p = c->E; p < c->P; ++p) {
+        if (now[p] == next[p]) continue;
+        const int src = next[p];
+        CK(cudaMemcpy(c->w1 + p * e1 * 8192, c->w1 + src * e1 * 8192, e1 * 8192, cudaMemcpyDeviceToDevice));
+        CK(cudaMemcpy(c->w1_sf + p * e1 * 512, c->w1_sf + src * e1 * 512, e1 * 512, cudaMemcpyDeviceToDevice));
+        CK(cudaMemcpy(c->w2 + p * e2 * 8192, c->w2 + src * e2 * 8192, e2 * 8192, cudaMemcpyDeviceToDevice));
+        CK(cudaMemcpy(c->w2_sf + p * e2 * 512, c->w2_sf + src * e2 * 512, e2 * 512, cudaMemcpyDeviceToDevice));
+    }
+    CK(cudaDeviceSynchronize());
+    return mm_set_eplb_map(c, pol.data(), rc.data(), max_replicas);
 }
 
 mm_status mm_bind_layer(mm_handle c, int layer)
@@ -345,10 +417,12 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->stamps = carve<uint64_t>(p, static_cast<size_t>(c->sms) * 8);
     c->ws = ws;
     c->ws_bytes = bytes;
-    if (!make_map(&c->maps.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox) ||
-        !make_map(&c->maps.hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->hq, I, rows, I, mm::kBBox)) {
-        free_ws(c);
-        return MM_ERR_CUDA;
+    for (int i = 0; i < mm::kTokBoxes; ++i) {
+        if (!make_map(&c->maps.xq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox << i) ||
+            !make_map(&c->maps.hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->hq, I, rows, I, mm::kBBox << i)) {
+            free_ws(c);
+            return MM_ERR_CUDA;
+        }
     }
     c->cap_tokens = max_tokens;
     c->rows_cap = rows;

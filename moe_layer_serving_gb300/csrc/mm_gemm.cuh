@@ -51,10 +51,11 @@ struct Unit {
     int expert;
     int row0;       // first dispatch row of the tile
     int rows;       // valid rows in the tile
-    int nbox;       // 16-row TMA boxes of token rows
     int nw;         // weight boxes of 128 rows (1 or 2): the MMA's N = 128 * nw
     int ksteps;
-    int wrb[2];     // row block (of 128) of each weight box in the stacked weights
+    int tbox;       // token box map: 16 << tbox rows (the smallest that covers the tile)
+    int wz;         // first weight block of the unit (K block 0); a stage adds 2 * ks
+    int m0;         // GEMM2: first output feature of the unit
 };
 
 // Token tiles the GEMMs run over (generic pointers: global or shared memory).
@@ -84,19 +85,17 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& g, const TileView& t
     un.expert = tv.expert[un.tile];
     un.row0 = tv.row0[un.tile];
     un.rows = tv.rows[un.tile];
-    un.nbox = (un.rows + kBBox - 1) / kBBox;
+    un.tbox = un.rows <= 16 ? 0 : (un.rows <= 32 ? 1 : (un.rows <= 64 ? 2 : 3));
     if (un.phase == 1) {
         un.nw = 2;
         un.ksteps = g.H / kKStep;
-        const int base = un.expert * (2 * g.I / kTile);
-        un.wrb[0] = base + un.blk;                  // gate rows
-        un.wrb[1] = base + g.I / kTile + un.blk;    // up rows
+        un.wz = (un.expert * nb1 + un.blk) * un.ksteps * 2;
+        un.m0 = 0;
     } else {
-        const int r0 = 2 * un.blk * kTile;
-        un.nw = (r0 + kTile < g.H) ? 2 : 1;
+        un.m0 = 2 * un.blk * kTile;
+        un.nw = (un.m0 + kTile < g.H) ? 2 : 1;
         un.ksteps = g.I / kKStep;
-        un.wrb[0] = (un.expert * g.H + r0) / kTile;
-        un.wrb[1] = un.wrb[0] + 1;
+        un.wz = (un.expert * nb2 + un.blk) * un.ksteps * 2;
     }
     return true;
 }
@@ -150,8 +149,7 @@ __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps
         fence_mbar_init();
         prefetch_tmap(&maps.w1);
         prefetch_tmap(&maps.w2);
-        prefetch_tmap(&maps.xq);
-        prefetch_tmap(&maps.hq);
+        prefetch_tmap(&maps.w2_one);
     }
     if (warp == 1) {
         tmem_alloc(s.tmem_slot, kTmemCols);
@@ -186,8 +184,8 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
     for (int i = 0; i < kStages; ++i) armed[i] = -1;
     Unit un;
     for (int u = first_unit; decode_unit(g, tv, u, un) && !*s.abort_flag; u += unit_stride) {
-        const CUtensorMap* wmap = un.phase == 1 ? &maps.w1 : &maps.w2;
-        const CUtensorMap* amap = un.phase == 1 ? &maps.xq : &maps.hq;
+        const CUtensorMap* wmap = un.phase == 1 ? &maps.w1 : (un.nw == 2 ? &maps.w2 : &maps.w2_one);
+        const CUtensorMap* amap = un.phase == 1 ? &maps.xq[un.tbox] : &maps.hq[un.tbox];
         const uint8_t* wsf = un.phase == 1 ? g.w1_sf : g.w2_sf;
         const uint8_t* asf = un.phase == 1 ? g.xs_t : g.hs_t;
         if (un.phase == 2) {
@@ -206,23 +204,20 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
             fence_proxy_async_global();
             if (*s.abort_flag) break;
         }
-        const uint32_t bytes = un.nbox * kBBox * kKStep + un.nw * kWBoxTxBytes + (1 + un.nw) * kSFBytes;
+        const uint32_t bytes = (kBBox << un.tbox) * kKStep + un.nw * kWBoxTxBytes + (1 + un.nw) * kSFBytes;
         for (int ks = 0; ks < un.ksteps; ++ks) {
             if (!mbar_wait(&s.empty[stage], phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
             uint8_t* st = s.stages + stage * kStageBytes;
             uint8_t* sf = st + kABytes + 2 * kWBoxBytes;
             mbar_arrive_expect_tx(&s.full[stage], bytes);
             armed[stage] = static_cast<int>(phase);
-            for (int bx = 0; bx < un.nbox; ++bx)
-                tma_load_2d(st + bx * kBBox * kKStep, amap, ks * kKStep, un.row0 + bx * kBBox, &s.full[stage],
-                            pol_a);
+            // four copies per stage: token rows, token scales, the weight block
+            // pair, the pair's scales
+            tma_load_2d(st, amap, ks * kKStep, un.row0, &s.full[stage], pol_a);
             bulk_load(sf, asf + (static_cast<int64_t>(un.tile) * un.ksteps + ks) * kSFBytes, kSFBytes, &s.full[stage]);
-            for (int w = 0; w < un.nw; ++w) {
-                tma_load_3d(st + kABytes + w * kWBoxBytes, wmap, 0, 0, un.wrb[w] * un.ksteps + ks, &s.full[stage],
-                            pol_w);
-                bulk_load(sf + (1 + w) * kSFBytes, wsf + (static_cast<int64_t>(un.wrb[w]) * un.ksteps + ks) * kSFBytes,
-                          kSFBytes, &s.full[stage]);
-            }
+            const int wz = un.wz + 2 * ks;
+            tma_load_3d(st + kABytes, wmap, 0, 0, wz, &s.full[stage], pol_w);
+            bulk_load(sf + kSFBytes, wsf + static_cast<int64_t>(wz) * kSFBytes, un.nw * kSFBytes, &s.full[stage]);
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -381,7 +376,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView&
             tc_fence_before();
             mbar_arrive(s.tmem_empty);
             if (active && cols && row_ok) {
-                const int m0 = (un.wrb[0] * kTile - un.expert * g.H) + half * kTile;   // first output feature
+                const int m0 = un.m0 + half * kTile;                                    // first output feature
                 uint4* dst = reinterpret_cast<uint4*>(g.y + static_cast<int64_t>(un.row0 + r) * g.H + m0);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {

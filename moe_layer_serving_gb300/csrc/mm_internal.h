@@ -41,26 +41,57 @@ constexpr int kWBoxTxBytes = kTile * kKStep / 2;     // what the TMA counts: the
 constexpr int kSFBytes = 512;                        // 128 rows x 4 scale bytes
 constexpr int kStageBytes = kABytes + 2 * kWBoxBytes + 4 * kSFBytes;
 
-// Scale-factor tile layout, shared by weights and activations.  Rows are
-// grouped by 128 and K by 128 (4 scale bytes per row); each group is one
-// 512-byte tile in which row r, scale byte b sits at
-//     (r % 32) * 16 + ((r % 128) / 32) * 4 + b
-// -- the order in which tcgen05.cp 32x128b.warpx4 places scales in tensor
-// memory for the block-scaled MMA (one 32-bit column per 32-row quarter).
-__host__ __device__ inline int64_t sf_tile_offset(int64_t row, int kblock32, int kchunks)
+// Weight blocks.  A weight block is 128 rows x 128 K of one expert.  Blocks
+// are stored in GEMM-unit order: expert, group (the unit's pair of 128-row
+// blocks), K block, then the pair's two members side by side, so one 3-D TMA
+// box (z extent 2) and one 1 KB bulk copy fetch a unit's whole stage.
+//   W1 (rows_per_expert = 2I): group = n-block nb, member 0 = the gate rows
+//       [nb*128, +128), member 1 = the up rows [I + nb*128, +128);
+//   W2 (rows_per_expert = H): group = m-block mb, members = rows
+//       [mb*256, +128) and [mb*256 + 128, +128) (the second is absent when
+//       H % 256 == 128 and mb is the last group).
+struct WOrder {
+    int rows_per_expert;
+    int groups;       // groups per expert
+    int kblocks;      // K / 128
+    int gate_up;      // 1: W1 pairing, 0: W2 pairing
+};
+
+__host__ __device__ inline int64_t w_block(const WOrder& o, int64_t row, int kb)
 {
-    const int64_t rb = row / 128;
-    const int kc = kblock32 / 4;
-    return (rb * kchunks + kc) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + (kblock32 % 4);
+    const int64_t p = row / o.rows_per_expert;
+    const int lrb = static_cast<int>((row % o.rows_per_expert) / 128);
+    int group, member;
+    if (o.gate_up) {
+        const int half_blocks = o.rows_per_expert / 256;
+        group = lrb % half_blocks;
+        member = lrb / half_blocks;
+    } else {
+        group = lrb / 2;
+        member = lrb % 2;
+    }
+    return ((p * o.groups + group) * o.kblocks + kb) * 2 + member;
 }
 
-// Weight tile layout: the packed e2m1 bytes of each (128-row block, 128-wide K
-// block) form one contiguous 8 KB tile, rows of 64 bytes, tiles ordered by row
-// block then K block, so one TMA box is one sequential 8 KB read of HBM.
-__host__ __device__ inline int64_t w_tile_offset(int64_t row, int64_t byte_col, int kblocks)
+// Packed e2m1 bytes: each block is one contiguous 8 KB tile, rows of 64 bytes,
+// so a TMA box reads sequential HBM.
+__host__ __device__ inline int64_t w_tile_offset(const WOrder& o, int64_t row, int64_t byte_col)
 {
-    return ((row / 128) * kblocks + byte_col / 64) * 8192 + (row % 128) * 64 + (byte_col % 64);
+    return w_block(o, row, static_cast<int>(byte_col / 64)) * 8192 + (row % 128) * 64 + (byte_col % 64);
 }
+
+// e8m0 scales: one 512-byte scale tile per block, in which row r, scale byte b
+// (the 32-wide K block b of the block's 128) sits at (r%32)*16 + ((r%128)/32)*4
+// + b -- the order in which tcgen05.cp 32x128b.warpx4 places scales in tensor
+// memory for the block-scaled MMA (one 32-bit column per 32-row quarter).
+__host__ __device__ inline int64_t w_sf_offset(const WOrder& o, int64_t row, int kblock32)
+{
+    return w_block(o, row, kblock32 / 4) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + (kblock32 % 4);
+}
+
+inline WOrder w1_order(int H, int I) { return WOrder{2 * I, I / 128, H / 128, 1}; }
+inline WOrder w2_order(int H, int I) { return WOrder{H, (H + 255) / 256, I / 128, 0}; }
+inline int64_t w_blocks(const WOrder& o, int P) { return static_cast<int64_t>(P) * o.groups * o.kblocks * 2; }
 
 // Activation scale tiles are per token tile: tile t, row r of the tile
 // (r < 128), 32-element block b along K.
@@ -72,16 +103,19 @@ __host__ __device__ inline int64_t act_sf_offset(int64_t tile, int r, int kblock
 __host__ __device__ inline int seg_rows(int cnt) { return (cnt + kSegAlign - 1) / kSegAlign * kSegAlign; }
 __host__ __device__ inline int tiles_of(int cnt) { return (cnt + kTokTile - 1) / kTokTile; }
 
+constexpr int kTokBoxes = 4;     // token-operand maps with boxes of 16, 32, 64, 128 rows
+
 struct GemmMaps {
-    CUtensorMap w1;   // e2m1 tiles [P*2I/128 * H/128][128 rows][128]  (16 x 4-bit -> 16-byte smem units)
-    CUtensorMap w2;   // e2m1 tiles [P*H/128 * I/128][128 rows][128]
-    CUtensorMap xq;   // e4m3 [rows][H]
-    CUtensorMap hq;   // e4m3 [rows][I]
+    CUtensorMap w1;            // W1 blocks, box = the unit's block pair (z extent 2)
+    CUtensorMap w2;            // W2 blocks, box = block pair
+    CUtensorMap w2_one;        // W2 blocks, box = one block (ragged last group)
+    CUtensorMap xq[kTokBoxes]; // e4m3 [rows][H], box 16 << i rows
+    CUtensorMap hq[kTokBoxes]; // e4m3 [rows][I], box 16 << i rows
 };
 
 struct GemmArgs {
-    const uint8_t* w1_sf;   // tiled [P][2I/128][H/128][512]
-    const uint8_t* w2_sf;   // tiled [P][H/128][I/128][512]
+    const uint8_t* w1_sf;   // scale tiles, one 512-byte tile per W1 block
+    const uint8_t* w2_sf;   // scale tiles, one per W2 block
     const uint8_t* xs_t;    // per token tile [tiles][H/128][512]
     uint8_t* hq;            // [rows][I]
     uint8_t* hs_t;          // per token tile [tiles][I/128][512]
@@ -109,6 +143,7 @@ struct mm_ctx {
     // EPLB map
     int32_t *map = nullptr, *rc = nullptr;
     int R = 1;
+    std::vector<int32_t> host_map, host_rc;   // the installed map, host copy (rebalancing)
     bool map_set = false;
     // per-layer logical counts [MM_MAX_LAYERS][E]
     int64_t* counts = nullptr;
@@ -154,8 +189,8 @@ cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s);
 cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s);
 cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s);
-cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s);
-cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s);
+cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
+cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
 cudaError_t gemm_prepare(int dev);
 cudaError_t small_prepare();
 cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logits, const float* bias, void* out,

@@ -186,25 +186,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     combine_chunk(y, w, pos, t, static_cast<int>(g % nc), H, k, out);
 }
 
-__global__ void tile_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K)
+__global__ void tile_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K,
+                                   WOrder o)
 {
     const int nb = K / 32;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (g >= rows * nb) return;
     const int64_t r = g / nb;
     const int b = static_cast<int>(g % nb);
-    dst[sf_tile_offset(r, b, K / 128)] = src[g];
+    dst[w_sf_offset(o, r, b)] = src[g];
 }
 
 // packed e2m1 [rows][K/2] -> 8 KB weight tiles, 16 bytes per thread
-__global__ void tile_weights_kernel(const uint4* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K)
+__global__ void tile_weights_kernel(const uint4* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K,
+                                    WOrder o)
 {
     const int per_row = K / 32;                    // 16-byte pieces per row
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (g >= rows * per_row) return;
     const int64_t r = g / per_row;
     const int c = static_cast<int>(g % per_row) * 16;
-    *reinterpret_cast<uint4*>(dst + w_tile_offset(r, c, K / 128)) = src[g];
+    *reinterpret_cast<uint4*>(dst + w_tile_offset(o, r, c)) = src[g];
 }
 
 unsigned grid_for(int64_t threads, int block) { return static_cast<unsigned>((threads + block - 1) / block); }
@@ -268,17 +270,17 @@ cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s
     return cudaGetLastError();
 }
 
-cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s)
+cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s)
 {
     const int64_t threads = rows * (K / 32);
-    tile_weights_kernel<<<grid_for(threads, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), dst, rows, K);
+    tile_weights_kernel<<<grid_for(threads, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), dst, rows, K, o);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, cudaStream_t s)
+cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s)
 {
     const int64_t threads = rows * (K / 32);
-    tile_scales_kernel<<<grid_for(threads, 256), 256, 0, s>>>(src, dst, rows, K);
+    tile_scales_kernel<<<grid_for(threads, 256), 256, 0, s>>>(src, dst, rows, K, o);
     return cudaGetLastError();
 }
 

@@ -249,3 +249,29 @@ def threads() -> int:
     """OpenMP threads the oracle will use (OMP_NUM_THREADS or all cores)."""
     v = os.environ.get("OMP_NUM_THREADS")
     return int(v) if v else (os.cpu_count() or 1)
+
+
+def plan_replicas(load, num_physical, max_replicas):
+    """EPLB replica plan.
+
+    Every logical expert e keeps physical slot e; the redundant slots E..P-1 are
+    handed out one at a time, each to the expert whose recorded load per replica
+    is highest (exact rational comparison; the lower index on ties), among the
+    experts that are below max_replicas.  The pages rebalance periodically from
+    the recorder's per-expert statistics ("sglang PR #35619", EPLB arm
+    settings) but do not spell out the placement rule; this greedy rule is the
+    reading taken here.  Returns (phys_of_logical [E, R] with -1 for unused
+    entries, replica_counts [E]).
+    """
+    from fractions import Fraction
+    load = [int(v) for v in np.asarray(load).ravel()]
+    E = len(load)
+    pol = np.full((E, max_replicas), -1, np.int32)
+    rc = np.ones(E, np.int32)
+    pol[:, 0] = np.arange(E)
+    for slot in range(E, num_physical):
+        cands = [e for e in range(E) if rc[e] < max_replicas]
+        best = max(cands, key=lambda e: (Fraction(load[e], int(rc[e])), -e))
+        pol[best, rc[best]] = slot
+        rc[best] += 1
+    return pol, rc

@@ -203,3 +203,28 @@ def test_routing_bit_exact_wide_experts(torch):
     idx, w = oracle.route(logits, bias, cfg.k)
     assert np.array_equal(res["idx"], idx)
     assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [400, 1500])
+def test_rebalance_keeps_outputs_and_spreads_load(torch, T):
+    # skewed routing, replicas first placed on experts 0..3; recorded counts
+    # drive a new plan with up to 4 replicas per expert
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], P=12, zipf_s=1.4, recording=True)
+    hidden, logits, bias = synthetic.make_activations(cfg, T)
+    run = gpu_util.Run(cfg, cap=T)
+    run.op.set_recording(True)
+    r1 = run.forward(hidden, logits, bias)
+    counts = run.op.read_counts(0)
+    run.op.rebalance(0, 4)
+    run.op.set_recording(False)
+    r2 = run.forward(hidden, logits, bias)
+    run.close()
+    assert r1["status"] == 0 and r2["status"] == 0
+    assert np.array_equal(r1["idx"], r2["idx"])
+    assert not np.array_equal(r1["phys"], r2["phys"])          # the map really changed
+    assert np.array_equal(r1["out"], r2["out"])                # replicas are byte copies
+    load1 = np.bincount(r1["phys"].ravel(), minlength=cfg.P)
+    load2 = np.bincount(r2["phys"].ravel(), minlength=cfg.P)
+    assert load2.max() < load1.max()
+    pol, rc = oracle.plan_replicas(counts, cfg.P, 4)
+    assert np.array_equal(r2["phys"], oracle.eplb(r2["idx"], pol, rc))

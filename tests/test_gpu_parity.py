@@ -68,3 +68,17 @@ def test_config3_prefill_t8192():
 
 def test_config4_skewed_eplb_t16384():
     _cfg_run(4, sample=16)
+
+
+def test_ragged_hidden_and_odd_shapes():
+    # H = 384: the last GEMM2 block has 128 output features (one weight block);
+    # I = 256: two GEMM1 n-blocks; 37 tokens spread over 6 experts, top-3
+    import dataclasses
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=37, H=384, I=256, E=6, P=6, k=3)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    W = synthetic.make_all_weights(cfg)
+    run = gpu_util.Run(cfg, W, cap=cfg.T)
+    res = run.forward(hidden, logits, bias)
+    run.close()
+    assert res["status"] == 0
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None)
