@@ -34,6 +34,34 @@ METRIC = "MoE-layer tokens/s"
 EXPERT_BYTES_PER_ELEM = 0.5 + 1.0 / 32      # packed e2m1 + one e8m0 byte per 32
 
 
+def sources_digest() -> str:
+    """sha256 over the kernel sources (csrc/*.cu, *.cuh, *.h and the C header)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "moe_layer_serving_gb300", "csrc")
+    files = sorted(os.path.join("moe_layer_serving_gb300", "csrc", f) for f in os.listdir(csrc)
+                   if f.endswith((".cu", ".cuh", ".h")))
+    files.append(os.path.join("include", "megamoe.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None when there is none or the kernel
+    sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    entry = json.load(open(path)).get(kernel, {}).get(workload)
+    if not entry or entry.get("sources_sha256") != sources_digest():
+        return None
+    return entry["bytes_per_launch"]
+
+
 def expert_bytes(cfg) -> int:
     return int((2 * cfg.I * cfg.H + cfg.H * cfg.I) * EXPERT_BYTES_PER_ELEM)
 
@@ -113,6 +141,22 @@ def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens):
     oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel)
     dt = time.perf_counter() - t0
     return sel.size / dt, dt, sel.size
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank processed its own batch in at most max_ms."""
+    return tokens_per_rank * world / (max_ms / 1e3)
 
 
 def dist_setup():
@@ -225,15 +269,10 @@ def main():
     clk = clocks.stop()
     torch.cuda.synchronize()
     barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
     kern_ms = float(np.mean(kern))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     assert op.get_status() == 0
-    value = cfg.T * world / (ms / 1e3)
+    value = weak_scaling_value(cfg.T, world, ms)
 
     # ---- end to end through the public call, host buffers ------------------
     xh = torch.from_numpy(hidden.view(np.int16)).pin_memory()
@@ -252,13 +291,8 @@ def main():
             oh.copy_(out.view(torch.int16), non_blocking=True)
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = cfg.T * world / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e = weak_scaling_value(cfg.T, world, e2e_ms)
     h2d = hidden.nbytes + logits.nbytes
     d2h = cfg.T * cfg.H * 2
 
@@ -271,15 +305,19 @@ def main():
         alg = touched * expert_bytes(cfg)           # weight streaming: the touched experts' bytes
         achieved = alg / (kern_ms / 1e3) / 1e9
         peak = peaks.get("hbm_gbs", 6800.0)
+        kname = "small_kernel" if route == 1 else "gemm_kernel"
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "gemm_kernel", "algorithmic_bytes": alg,
+                "traffic": measured_traffic(kname, workload_config(cfg)["workload"]), "kernel": kname,
+                "algorithmic_bytes": alg,
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
     else:
         flops = 6.0 * cfg.T * cfg.k * cfg.H * cfg.I
         achieved = flops / (kern_ms / 1e3) / 1e12
         peak = peaks.get("bf16_tflops", 1900.0) * 2.0   # fp8-class MMA: 2x the bf16 rate
+        kname = "small_kernel" if route == 1 else "gemm_kernel"
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "gemm_kernel", "algorithmic_flops": flops,
+                "traffic": measured_traffic(kname, workload_config(cfg)["workload"]), "kernel": kname,
+                "algorithmic_flops": flops,
                 "peak_source": "measured bf16 x 2" if "bf16_tflops" in peaks else "fallback x 2"}
 
     line = {

@@ -158,6 +158,11 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
     c->k = k;
     c->H = H;
     c->I = I;
+    {
+        const char* f = getenv("MM_FAULT");
+        if (f && !strcmp(f, "grid_barrier")) c->fault = mm::kFaultGridBarrier;
+        else if (f && !strcmp(f, "gemm_dependency")) c->fault = mm::kFaultGemmDependency;
+    }
     c->small_max = env_int("MM_SMALL_M_MAX", mm::kSmallMaxTokens);
     if (c->small_max > mm::kSmallMaxTokens) c->small_max = mm::kSmallMaxTokens;
     c->large_min = env_int("MM_LARGE_M_MIN", 1024);

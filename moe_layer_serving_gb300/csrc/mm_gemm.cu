@@ -55,6 +55,7 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.I = c->I;
     g.P = c->P;
     g.phases = 3;
+    g.fault = c->fault;
 }
 
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)

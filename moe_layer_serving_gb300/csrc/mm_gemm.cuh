@@ -189,7 +189,7 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
         const uint8_t* wsf = un.phase == 1 ? g.w1_sf : g.w2_sf;
         const uint8_t* asf = un.phase == 1 ? g.xs_t : g.hs_t;
         if (un.phase == 2) {
-            const int need = g.I / kTile;
+            const int need = g.I / kTile + (g.fault == kFaultGemmDependency ? 1 : 0);
             if (ld_acquire(&g.done1[un.tile]) < need) {
                 const uint64_t t0 = globaltimer();
                 while (ld_acquire(&g.done1[un.tile]) < need) {

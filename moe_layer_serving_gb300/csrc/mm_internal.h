@@ -128,6 +128,7 @@ struct GemmArgs {
     int* status;
     int H, I, P;
     int phases;             // bit 0: GEMM1 units, bit 1: GEMM2 units
+    int fault;              // injected fault (FaultSite), 0 = none
 };
 
 }  // namespace mm
@@ -137,6 +138,7 @@ struct mm_ctx {
     int E = 0, P = 0, k = 0, H = 0, I = 0;
     int small_max = 512, large_min = 1024;
     int route = MM_ROUTE_AUTO, layer = 0, recording = 0;
+    int fault = 0;                  // mm::FaultSite
     // weights (library-owned)
     uint8_t *w1 = nullptr, *w1_sf = nullptr, *w2 = nullptr, *w2_sf = nullptr;
     bool weights_set = false;
@@ -181,6 +183,16 @@ enum WaitSite {
     kSiteEpiTmemFull = 4,
     kSiteProducerDone1 = 5,
     kSiteGridBarrier = 6,
+};
+
+// Fault injection for the failure-detection tests (environment variable
+// MM_FAULT, read at mm_create).  Each one only makes a bounded device-side wait
+// unsatisfiable -- no invalid access, trap or endless loop -- so the wait must
+// give up, latch MM_ERR_TIMEOUT with its site, and leave the context usable.
+enum FaultSite {
+    kFaultNone = 0,
+    kFaultGridBarrier = 1,   // CTA 0 withholds its arrival at the fused kernel's second grid barrier
+    kFaultGemmDependency = 2 // GEMM2 units wait for one GEMM1 unit more than a tile has
 };
 
 // host-side launchers (return cudaGetLastError of the launch)

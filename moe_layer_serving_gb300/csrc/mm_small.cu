@@ -59,13 +59,13 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
 
 // Sense-counting grid barrier: the last CTA to arrive resets the count and
 // bumps the generation; the others wait (bounded) for the bump.
-__device__ bool grid_sync(unsigned* bar, int* status, volatile int* abort_flag)
+__device__ bool grid_sync(unsigned* bar, int* status, volatile int* abort_flag, bool withhold = false)
 {
     __syncthreads();
     if (threadIdx.x == 0 && !*abort_flag) {
         const unsigned gen = ld_acquire_u32(bar + 1);
         __threadfence();
-        if (atomicAdd(bar, 1u) + 1u == gridDim.x) {
+        if (!withhold && atomicAdd(bar, 1u) + 1u == gridDim.x) {
             atomicExch(bar, 0u);
             __threadfence();
             atomicAdd(bar + 1, 1u);
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_proxy_async_shared();     // scratch writes above precede the TMA writes into the same buffers
     if (threadIdx.x == 0) stamp[3] = globaltimer();
-    ok = grid_sync(a.bar, g.status, s.abort_flag);
+    ok = grid_sync(a.bar, g.status, s.abort_flag, g.fault == kFaultGridBarrier && blockIdx.x == 0);
     if (threadIdx.x == 0) stamp[4] = globaltimer();
 
     // ---- F: GEMM1 + SwiGLU + requant, GEMM2 (tiles from shared memory) -----

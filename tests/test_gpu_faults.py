@@ -1,0 +1,64 @@
+"""Failure detection without a GPU fault.
+
+MM_FAULT (read when a handle is created) makes one device-side wait
+unsatisfiable: one CTA withholds its arrival at a grid barrier of the fused
+kernel, or GEMM2 waits for a GEMM1 unit that never exists.  Every wait in the
+kernels is bounded, so the forward must come back with MM_ERR_TIMEOUT latched
+and the site that raised it, and the CUDA context must stay usable: a handle
+without the fault then runs the same layer and matches the oracle.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+SITE_PRODUCER_DONE1, SITE_GRID_BARRIER = 5, 6
+
+
+@pytest.fixture(scope="module")
+def torch():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    return torch
+
+
+def _faulty_run(cfg, T, fault):
+    os.environ["MM_FAULT"] = fault
+    try:
+        run = gpu_util.Run(cfg, cap=T)
+    finally:
+        del os.environ["MM_FAULT"]
+    hidden, logits, bias = synthetic.make_activations(cfg, T)
+    res = run.forward(hidden, logits, bias, dumps=False)
+    route, _, site = run.op.last_info()
+    run.close()
+    return res["status"], route, site, (hidden, logits, bias)
+
+
+@pytest.mark.parametrize("fault,T,site,route", [("grid_barrier", 64, SITE_GRID_BARRIER, 1),
+                                                ("gemm_dependency", 64, SITE_PRODUCER_DONE1, 1),
+                                                ("gemm_dependency", 1200, SITE_PRODUCER_DONE1, 2)])
+def test_injected_wait_times_out_and_context_survives(torch, fault, T, site, route):
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    status, took, got_site, inputs = _faulty_run(cfg, T, fault)
+    assert took == route
+    assert status == mm.MM_ERR_TIMEOUT
+    assert got_site == site
+    # the context is still usable: a clean handle runs the layer correctly
+    run = gpu_util.Run(cfg, cap=T)
+    res = run.forward(*inputs, dumps=False)
+    run.close()
+    assert res["status"] == 0
+    ref = oracle.forward(*inputs, cfg.k, gpu_util.weights(cfg))
+    gpu_util.assert_out_close(res["out"], ref["out"])
