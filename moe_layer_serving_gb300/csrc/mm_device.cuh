@@ -16,9 +16,14 @@ namespace mm {
 // ---------------------------------------------------------------------------
 // status latch and bounded waits
 // ---------------------------------------------------------------------------
-// Every spin-wait gives up after this many nanoseconds of %globaltimer and
-// latches MM_ERR_TIMEOUT; kernels then drain and return instead of hanging.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// Every spin-wait gives up after a bounded time of %globaltimer and latches
+// MM_ERR_TIMEOUT with its site; kernels then drain and return instead of
+// hanging.  Waits on progress made elsewhere (grid barriers, GEMM1 -> GEMM2
+// dependencies) give up first; waits inside a CTA's own pipeline (mbarriers)
+// get twice as long, so that the site reported is the root cause and not a
+// stage starved by it.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;          // 2 s: external progress
+constexpr uint64_t kPipeWaitLimitNs = 2 * kWaitLimitNs;   // 4 s: own pipeline
 
 __device__ __forceinline__ uint64_t globaltimer()
 {
@@ -84,7 +89,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > kPipeWaitLimitNs) {
             latch_error(status, MM_ERR_TIMEOUT, site);
             *abort = 1;
             return false;
