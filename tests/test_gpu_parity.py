@@ -82,3 +82,36 @@ def test_ragged_hidden_and_odd_shapes():
     run.close()
     assert res["status"] == 0
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None)
+
+
+def test_maximum_experts_and_topk_small_path():
+    # E = P = 512 (the limit), top-8, T = 512 (the fused kernel's limit)
+    import dataclasses
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=512, H=256, I=128, E=512, P=512, k=8, bias_std=0.1)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    W = synthetic.make_all_weights(cfg)
+    run = gpu_util.Run(cfg, W, cap=cfg.T)
+    res = run.forward(hidden, logits, bias)
+    assert run.op.last_info()[:2] == (1, 1)
+    run.close()
+    assert res["status"] == 0
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(cfg.T, 48))
+
+
+@pytest.mark.parametrize("T", [512, 513])
+def test_concentrated_routing_many_tiles_per_expert(T):
+    # every token prefers the same 8 experts: 8 segments of T rows each, several
+    # 128-row tiles per expert, the rest of the experts idle
+    import dataclasses
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T, H=256, I=256, E=64, P=64, k=8)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    logits[:, :8] += 20.0
+    W = synthetic.make_all_weights(cfg)
+    run = gpu_util.Run(cfg, W, cap=T)
+    res = run.forward(hidden, logits, bias)
+    route = run.op.last_info()[0]
+    run.close()
+    assert route == (1 if T <= 512 else 2)
+    assert res["status"] == 0
+    assert np.all(np.sort(res["idx"], axis=1) == np.arange(8))
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(T, 40))
