@@ -160,10 +160,11 @@ def test_deterministic_across_runs(torch):
     assert np.array_equal(o1, o2)
 
 
-def test_graph_capture_replay_matches_eager(torch):
+@pytest.mark.parametrize("T", [96, 1100])          # fused small path, and the 7-launch large path
+def test_graph_capture_replay_matches_eager(torch, T):
     cfg = synthetic.CONFIGS[0]
-    hidden, logits, bias = synthetic.make_activations(cfg, 96)
-    run = gpu_util.Run(cfg, cap=96)
+    hidden, logits, bias = synthetic.make_activations(cfg, T)
+    run = gpu_util.Run(cfg, cap=T)
     x, lg, b = run.to_dev(hidden, logits, bias)
     eager = torch.empty_like(x)
     run.op.forward(x, lg, b, eager)
