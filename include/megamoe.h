@@ -178,7 +178,11 @@ MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t by
  * device-side timeout (0 none; see WaitSite in the sources)}.
  * Stage 11: uint64 [SMs][8] %globaltimer readings (ns) of each CTA of the last
  * fused small-input launch at its stage boundaries: start, routed, past
- * barrier 1, dispatched, past barrier 2, GEMMs done, past barrier 3, end. */
+ * barrier 1, dispatched, past barrier 2, GEMMs done, past barrier 3, end.
+ * Stage 12: int32 [tiles][3] token tiles of the last forward, each {physical
+ * expert, first dispatch row, rows}: a segment is cut into tiles of 128 rows
+ * (large-input path) or of 64 or 128 rows (fused small-input kernel, which
+ * takes 64 unless that adds more than 1/16 to the number of tiles). */
 
 /* Size in bytes of a debug stage for the last forward (0 before any). */
 MM_API mm_status mm_debug_size(mm_handle h, int stage, size_t *bytes);

@@ -28,7 +28,7 @@ ROUTE_AUTO, ROUTE_SMALL, ROUTE_LARGE = 0, 1, 2
 DUMP_STAGES = {0: ("idx", np.int32), 1: ("weights", np.float32), 2: ("phys", np.int32), 3: ("pos", np.int32),
                4: ("offsets", np.int32), 5: ("xq", np.uint8), 6: ("xs", np.uint8), 7: ("hq", np.uint8),
                8: ("hs", np.uint8), 9: ("y", np.uint16), 10: ("info", np.int32),
-               11: ("stamps", np.uint64)}
+               11: ("stamps", np.uint64), 12: ("tiles", np.int32)}
 
 _p, _i32, _i64, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
 _SIGS = {

@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -373,7 +374,9 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     // each non-empty segment adds < kSegAlign pad rows and < 1 partial token tile
     const int64_t busy = npairs < c->P ? npairs : c->P;
     const int64_t rows = npairs + busy * (mm::kSegAlign - 1) + mm::kSegAlign;
-    const int64_t tiles = npairs / mm::kTokTile + busy + 1;
+    // token tiles: kTokTile rows on the large-input path, kSmallTile rows in the fused kernel
+    const int64_t small_pairs = npairs < int64_t(mm::kSmallMaxTokens) * c->k ? npairs : int64_t(mm::kSmallMaxTokens) * c->k;
+    const int64_t tiles = std::max(npairs / mm::kTokTile, small_pairs / mm::kSmallTile) + busy + 1;
     const int64_t chunks = (npairs + mm::kChunkPairs - 1) / mm::kChunkPairs;
     const int64_t H = c->H, I = c->I;
     // size pass, then carve
@@ -555,6 +558,12 @@ static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* 
         case 9: *bytes = static_cast<size_t>(rows) * c->H * 2; break;
         case 10: *bytes = 3 * sizeof(int32_t); break;
         case 11: *bytes = static_cast<size_t>(c->sms) * 8 * sizeof(uint64_t); break;
+        case 12: {
+            int32_t ntiles = 0;
+            CK(cudaMemcpy(&ntiles, c->num_tiles, sizeof(int32_t), cudaMemcpyDeviceToHost));
+            *bytes = static_cast<size_t>(ntiles) * 3 * sizeof(int32_t);
+            break;
+        }
         default: return MM_ERR_INVALID_ARG;
     }
     return MM_OK;
@@ -581,6 +590,17 @@ mm_status mm_debug_dump(mm_handle c, int stage, void* dst, size_t bytes)
         CK(cudaMemcpy(&site, c->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost));
         const int32_t info[3] = {c->last_route, c->last_launches, site ? site : c->last_site};
         memcpy(dst, info, n);
+        return MM_OK;
+    }
+    if (stage == 12) {
+        const size_t ntiles = full / (3 * sizeof(int32_t));
+        std::vector<int32_t> cols(3 * ntiles), table(3 * ntiles);
+        CK(cudaMemcpy(cols.data(), c->tile_expert, ntiles * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CK(cudaMemcpy(cols.data() + ntiles, c->tile_row0, ntiles * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CK(cudaMemcpy(cols.data() + 2 * ntiles, c->tile_rows, ntiles * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        for (size_t t = 0; t < ntiles; ++t)
+            for (int j = 0; j < 3; ++j) table[3 * t + j] = cols[j * ntiles + t];
+        memcpy(dst, table.data(), n);
         return MM_OK;
     }
     const void* src = nullptr;

@@ -129,6 +129,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// Ask for global bytes to be brought into L2 (no completion, no destination).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
@@ -194,6 +201,27 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
+}
+
+// The same MMA with a compile-time accumulate flag: no predicate to compute
+// in the issuing thread.  The issuing thread's own instruction count per MMA
+// sets the MMA rate when the operands are small, so the K loop keeps to this form.
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_mxf8f6f4_c(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem)
+{
+    if (kAccumulate)
+        asm volatile(
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 1;" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 0;" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
 }
 
 // Arrive on an mbarrier once every prior tcgen05 operation of this thread completed.

@@ -10,21 +10,22 @@
 namespace mm {
 namespace {
 
-constexpr int kSmemBytes = kGemmSmemBytes + 1024;
+using Geo = GeomLarge;
+constexpr int kSmemBytes = Geo::kSmemBytes + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const GemmSmem s = gemm_smem(smem);
-    const uint32_t tmem = gemm_setup(s, maps);
+    const GemmSmem s = gemm_smem(smem, smem + Geo::kStageRegion);
+    const uint32_t tmem = gemm_setup<Geo>(s, maps);
     TileView tv;
     tv.expert = g.tile_expert;
     tv.row0 = g.tile_row0;
     tv.rows = g.tile_rows;
     tv.ntiles = *g.num_tiles;
-    gemm_roles(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+    gemm_roles<Geo>(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
     gemm_teardown(tmem);
 }
 
@@ -39,6 +40,8 @@ cudaError_t gemm_prepare(int dev)
 void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
 {
     GemmArgs& g = *gp;
+    g.w1 = c->w1;
+    g.w2 = c->w2;
     g.w1_sf = c->w1_sf;
     g.w2_sf = c->w2_sf;
     g.xs_t = c->xs_t;

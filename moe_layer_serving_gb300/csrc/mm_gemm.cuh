@@ -44,6 +44,28 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns: accumulator [0, 256), then the current stage's scale factors
 constexpr uint32_t kColSFA = 256, kColSFB = 260;   // SFB: 4 columns per 128 weight rows
 
+// Shared-memory pipeline geometry: token rows held per stage (the tile size
+// of the kernel's token tiles) and the number of stages.  The MMA reads 128
+// token rows whatever the tile size; rows past a short tile's region lie in
+// the same stage's weight region and only feed accumulator rows the epilogue
+// ignores.  The fused small-input kernel uses short tiles so that one more
+// stage fits: with few tokens per expert its time is the weight stream's,
+// set by how many bytes each SM keeps in flight.
+template <int kRows_, int kStages_>
+struct Geom {
+    static constexpr int kRows = kRows_;
+    static constexpr int kStages = kStages_;
+    static constexpr int kABytes = kRows * kKStep;
+    static constexpr int kStageBytes = kABytes + 2 * kWBoxBytes + 4 * kSFBytes;
+    static constexpr int kStageRegion = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kStageRegion + 256;   // stages + barriers
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static_assert(kRows % 16 == 0 && kRows <= 128, "token rows per stage");
+    static_assert(kStages <= 8, "barrier block holds eight stages");
+};
+using GeomLarge = Geom<kTokTile, MM_STAGES>;
+using GeomSmall = Geom<kSmallTile, MM_SMALL_STAGES>;
+
 struct Unit {
     int phase;      // 1 or 2
     int tile;
@@ -119,15 +141,17 @@ struct GemmSmem {
     uint32_t* tmem_slot;
     volatile int* abort_flag;
 };
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 256;   // stages + barriers
-
-__device__ __forceinline__ GemmSmem gemm_smem(uint8_t* smem)
+// Barrier block (256 bytes): full[8], empty[8], tmem_full, tmem_empty, the
+// TMEM base and the abort flag.  Its layout does not depend on the stage
+// count, so one kernel can run either geometry over the same buffers.
+constexpr int kMaxStages = 8;
+__device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
 {
     GemmSmem s;
-    s.stages = smem;
-    s.full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    s.empty = s.full + kStages;
-    s.tmem_full = s.empty + kStages;
+    s.stages = stages;
+    s.full = reinterpret_cast<uint64_t*>(bars);
+    s.empty = s.full + kMaxStages;
+    s.tmem_full = s.empty + kMaxStages;
     s.tmem_empty = s.tmem_full + 1;
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.tmem_empty + 1);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
@@ -135,11 +159,12 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* smem)
 }
 
 // All threads: barriers, tensor-memory allocation (warp 1); returns the TMEM base.
+template <class G>
 __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps& maps)
 {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < G::kStages; ++i) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
         }
@@ -173,6 +198,7 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem)
 }
 
 // ---- producer: one thread issues every TMA / bulk copy -----------------------
+template <class G>
 __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                               const GemmSmem& s, int first_unit, int unit_stride)
 {
@@ -180,6 +206,7 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
+    constexpr int kStages = G::kStages;
     int armed[kStages];
     for (int i = 0; i < kStages; ++i) armed[i] = -1;
     Unit un;
@@ -205,10 +232,18 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
             if (*s.abort_flag) break;
         }
         const uint32_t bytes = (kBBox << un.tbox) * kKStep + un.nw * kWBoxTxBytes + (1 + un.nw) * kSFBytes;
+        const uint8_t* wblk = (un.phase == 1 ? g.w1 : g.w2) + static_cast<int64_t>(un.wz) * kWBoxTxBytes;
+        if (kPrefetch > 0) {
+            // the first stages of the unit; later ones are requested kPrefetch stages ahead
+            for (int j = 1; j < kPrefetch && j < un.ksteps; ++j)
+                prefetch_l2(wblk + static_cast<int64_t>(2 * j) * kWBoxTxBytes, un.nw * kWBoxTxBytes);
+        }
         for (int ks = 0; ks < un.ksteps; ++ks) {
+            if (kPrefetch > 0 && ks + kPrefetch < un.ksteps)
+                prefetch_l2(wblk + static_cast<int64_t>(2 * (ks + kPrefetch)) * kWBoxTxBytes, un.nw * kWBoxTxBytes);
             if (!mbar_wait(&s.empty[stage], phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
-            uint8_t* st = s.stages + stage * kStageBytes;
-            uint8_t* sf = st + kABytes + 2 * kWBoxBytes;
+            uint8_t* st = s.stages + stage * G::kStageBytes;
+            uint8_t* sf = st + G::kABytes + 2 * kWBoxBytes;
             mbar_arrive_expect_tx(&s.full[stage], bytes);
             armed[stage] = static_cast<int>(phase);
             // four copies per stage: token rows, token scales, the weight block
@@ -216,7 +251,7 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
             tma_load_2d(st, amap, ks * kKStep, un.row0, &s.full[stage], pol_a);
             bulk_load(sf, asf + (static_cast<int64_t>(un.tile) * un.ksteps + ks) * kSFBytes, kSFBytes, &s.full[stage]);
             const int wz = un.wz + 2 * ks;
-            tma_load_3d(st + kABytes, wmap, 0, 0, wz, &s.full[stage], pol_w);
+            tma_load_3d(st + G::kABytes, wmap, 0, 0, wz, &s.full[stage], pol_w);
             bulk_load(sf + kSFBytes, wsf + static_cast<int64_t>(wz) * kSFBytes, un.nw * kSFBytes, &s.full[stage]);
             if (++stage == kStages) {
                 stage = 0;
@@ -236,9 +271,22 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
 }
 
 // ---- MMA issuer: one thread ---------------------------------------------------
+// Descriptors are built once; a stage only adds its offset (the address field
+// of a descriptor counts 16-byte units and every stage lies below 256 KB, so
+// the add never carries out of that field).  The instruction descriptors of a
+// unit are formed once per unit.
+template <class G>
 __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, const GemmSmem& s, uint32_t tmem,
                                          int first_unit, int unit_stride)
 {
+    const uint64_t a_desc0 = desc_kmajor_sw128(s.stages);
+    const uint64_t b_desc0 = desc_kmajor_sw128(s.stages + G::kABytes);
+    const uint64_t sf_desc0 = desc_sf(s.stages + G::kABytes + 2 * kWBoxBytes);
+    constexpr int kStages = G::kStages;
+    static_assert(kKStep == 4 * 32, "four MMAs of K = 32 per stage");
+    static_assert(kStages * G::kStageBytes + 1024 < (1 << 18), "descriptor address field");
+    constexpr uint64_t kStageDesc = G::kStageBytes >> 4, kSfDesc = kSFBytes >> 4;
+    const uint32_t t_sfa = tmem + kColSFA, t_sfb = tmem + kColSFB;
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     Unit un;
@@ -246,19 +294,24 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, 
         if (!mbar_wait(s.tmem_empty, acc_phase ^ 1u, g.status, s.abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
         const uint32_t n = static_cast<uint32_t>(un.nw * kTile);
+        const uint32_t id0 = idesc_e4m3_e2m1(n, 0), id1 = idesc_e4m3_e2m1(n, 1);
+        const uint32_t id2 = idesc_e4m3_e2m1(n, 2), id3 = idesc_e4m3_e2m1(n, 3);
+        const bool two = un.nw == 2;
         for (int ks = 0; ks < un.ksteps; ++ks) {
             if (!mbar_wait(&s.full[stage], phase, g.status, s.abort_flag, kSiteMmaFull)) break;
             tc_fence_after();
-            uint8_t* st = s.stages + stage * kStageBytes;
-            uint8_t* sf = st + kABytes + 2 * kWBoxBytes;
-            tc_cp_32x128b_x4(tmem + kColSFA, desc_sf(sf));
-            for (int w = 0; w < un.nw; ++w) tc_cp_32x128b_x4(tmem + kColSFB + 4 * w, desc_sf(sf + (1 + w) * kSFBytes));
-            const uint64_t adesc = desc_kmajor_sw128(st);
-            const uint64_t bdesc = desc_kmajor_sw128(st + kABytes);
-#pragma unroll
-            for (int kk = 0; kk < kKStep / 32; ++kk)
-                mma_mxf8f6f4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc_e4m3_e2m1(n, kk), tmem + kColSFA,
-                             tmem + kColSFB, (ks | kk) != 0 ? 1u : 0u);
+            const uint64_t off = static_cast<uint64_t>(stage) * kStageDesc;
+            const uint64_t ad = a_desc0 + off, bd = b_desc0 + off, sd = sf_desc0 + off;
+            tc_cp_32x128b_x4(t_sfa, sd);
+            tc_cp_32x128b_x4(t_sfb, sd + kSfDesc);
+            if (two) tc_cp_32x128b_x4(t_sfb + 4, sd + 2 * kSfDesc);
+            if (ks == 0)
+                mma_mxf8f6f4_c<false>(tmem, ad, bd, id0, t_sfa, t_sfb);
+            else
+                mma_mxf8f6f4_c<true>(tmem, ad, bd, id0, t_sfa, t_sfb);
+            mma_mxf8f6f4_c<true>(tmem, ad + 2, bd + 2, id1, t_sfa, t_sfb);
+            mma_mxf8f6f4_c<true>(tmem, ad + 4, bd + 4, id2, t_sfa, t_sfb);
+            mma_mxf8f6f4_c<true>(tmem, ad + 6, bd + 6, id3, t_sfa, t_sfb);
             tc_commit(&s.empty[stage]);
             if (++stage == kStages) {
                 stage = 0;
@@ -395,14 +448,15 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView&
 }
 
 // All threads: each warp runs its role over units first_unit, +unit_stride, ...
+template <class G>
 __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                            const GemmSmem& s, uint32_t tmem, int first_unit, int unit_stride)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 0) {
-        if (lane == 0) producer_loop(maps, g, tv, s, first_unit, unit_stride);
+        if (lane == 0) producer_loop<G>(maps, g, tv, s, first_unit, unit_stride);
     } else if (warp == 1) {
-        if (lane == 0) mma_loop(g, tv, s, tmem, first_unit, unit_stride);
+        if (lane == 0) mma_loop<G>(g, tv, s, tmem, first_unit, unit_stride);
     } else {
         epilogue_loop(g, tv, s, tmem, first_unit, unit_stride);
     }

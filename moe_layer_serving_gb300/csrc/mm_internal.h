@@ -14,32 +14,37 @@
 namespace mm {
 
 // ---- tile geometry --------------------------------------------------------
-// Both GEMMs put one token tile on the MMA's M side (128 rows, e4m3) and 256
-// weight rows on its N side (e2m1), K in stages of 128.  A block-scaled
-// tcgen05 MMA costs about the same time whatever its N, so every instruction
-// is issued at the full N = 256 (gate + up rows of 128 I-columns for GEMM1,
-// 256 output features for GEMM2).
+// Both GEMMs put one token tile on the MMA's M side (e4m3; the MMA is always
+// M = 128, rows past the tile are ignored) and 256 weight rows on its N side
+// (e2m1), K in stages of 128: gate + up rows of 128 I-columns for GEMM1, 256
+// output features for GEMM2.
 // Every physical expert's dispatched rows form a segment that starts at a
-// multiple of kSegAlign rows and is cut into token tiles of kTokTile rows, so
-// a tile never straddles two experts.
+// multiple of kSegAlign rows and is cut into token tiles (kTokTile rows on the
+// large-input path, kSmallTile rows in the fused small-input kernel), so a
+// tile never straddles two experts.
 #ifndef MM_STAGES
 #define MM_STAGES 4
 #endif
+#ifndef MM_SMALL_STAGES
+#define MM_SMALL_STAGES 5
+#endif
+#ifndef MM_PREFETCH
+#define MM_PREFETCH 2
+#endif
 constexpr int kTile = 128;       // weight rows per TMA box / weight row block
-constexpr int kTokTile = 128;    // token rows per tile (the MMA's M)
+constexpr int kTokTile = 128;    // token rows per tile, large-input path
+constexpr int kSmallTile = 64;   // token rows per tile, fused small-input kernel
 constexpr int kSegAlign = 16;    // segment start alignment (rows)
 constexpr int kKStep = 128;      // reduction elements per pipeline stage
 constexpr int kBBox = 16;        // token rows per TMA box of the token operand
-constexpr int kStages = MM_STAGES;  // shared-memory pipeline depth
+constexpr int kPrefetch = MM_PREFETCH;  // weight stages requested into L2 ahead of the TMA loads
 constexpr int kChunkPairs = 1024;  // (token, slot) pairs per permute chunk
 constexpr int kSmallMaxTokens = 512;  // largest batch the fused small-input kernel takes
 
 // shared-memory stage: tokens (A) | weights (B, two 128-row boxes) | SF(A, B0, B1)
-constexpr int kABytes = kTokTile * kKStep;           // e4m3 token rows
 constexpr int kWBoxBytes = kTile * kKStep;           // e2m1 unpacked to 1 byte/element in smem
 constexpr int kWBoxTxBytes = kTile * kKStep / 2;     // what the TMA counts: the packed global bytes
 constexpr int kSFBytes = 512;                        // 128 rows x 4 scale bytes
-constexpr int kStageBytes = kABytes + 2 * kWBoxBytes + 4 * kSFBytes;
 
 // Weight blocks.  A weight block is 128 rows x 128 K of one expert.  Blocks
 // are stored in GEMM-unit order: expert, group (the unit's pair of 128-row
@@ -101,7 +106,7 @@ __host__ __device__ inline int64_t act_sf_offset(int64_t tile, int r, int kblock
 }
 
 __host__ __device__ inline int seg_rows(int cnt) { return (cnt + kSegAlign - 1) / kSegAlign * kSegAlign; }
-__host__ __device__ inline int tiles_of(int cnt) { return (cnt + kTokTile - 1) / kTokTile; }
+__host__ __device__ inline int tiles_of(int cnt, int tile = kTokTile) { return (cnt + tile - 1) / tile; }
 
 constexpr int kTokBoxes = 4;     // token-operand maps with boxes of 16, 32, 64, 128 rows
 
@@ -114,6 +119,8 @@ struct GemmMaps {
 };
 
 struct GemmArgs {
+    const uint8_t* w1;      // weight blocks in unit order (packed e2m1, 8 KB per block)
+    const uint8_t* w2;
     const uint8_t* w1_sf;   // scale tiles, one 512-byte tile per W1 block
     const uint8_t* w2_sf;   // scale tiles, one per W2 block
     const uint8_t* xs_t;    // per token tile [tiles][H/128][512]

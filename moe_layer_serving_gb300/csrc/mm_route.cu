@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(const __nv_bfloat16
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = g / nb;
     if (t >= T) return;
-    quant_dispatch_block(x, t, static_cast<int>(g % nb), H, k, pos + t * k, phys + t * k, off, toff, xq, xs_t);
+    quant_dispatch_block(x, t, static_cast<int>(g % nb), H, k, pos + t * k, phys + t * k, off, toff, kTokTile, xq,
+                         xs_t);
 }
 
 // ---------------------------------------------------------------------------

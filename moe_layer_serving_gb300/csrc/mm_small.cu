@@ -30,8 +30,15 @@ namespace {
 
 constexpr int kSmallWarps = kThreads / 32;
 constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
-constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kTokTile + 1;
-constexpr int kSmallSmemBytes = kGemmSmemBytes + 3 * kMaxSmallTiles * 4 + 64 + 1024;
+// Two pipeline geometries over one buffer: short tiles with one more stage
+// when every expert's rows fit in few short tiles (weight streaming, where the
+// bytes in flight per SM set the rate), full tiles otherwise (fewer units,
+// each expert's weights streamed fewer times).
+constexpr int kStageRegion =
+    GeomSmall::kStageRegion > GeomLarge::kStageRegion ? GeomSmall::kStageRegion : GeomLarge::kStageRegion;
+constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kSmallTile + 1;
+constexpr int kSmallSmemBytes = kStageRegion + 256 + 3 * kMaxSmallTiles * 4 + 64 + 1024;
+static_assert(kSmallSmemBytes <= 232448, "shared memory per block");
 
 struct SmallArgs {
     RouteArgs route;
@@ -91,12 +98,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const GemmSmem s = gemm_smem(smem);
-    int* t_expert = reinterpret_cast<int*>(smem + kGemmSmemBytes);
+    const GemmSmem s = gemm_smem(smem, smem + kStageRegion);
+    int* t_expert = reinterpret_cast<int*>(smem + kStageRegion + 256);
     int* t_row0 = t_expert + kMaxSmallTiles;
     int* t_rows = t_row0 + kMaxSmallTiles;
-    int* scal = t_rows + kMaxSmallTiles;            // [0] tiles, [1] rows
-    const uint32_t tmem = gemm_setup(s, maps);
+    int* scal = t_rows + kMaxSmallTiles;            // [0] tiles, [1] rows, [2] [3] tile counts
+    static_assert(GeomSmall::kStages >= GeomLarge::kStages, "barriers initialised for the deeper pipeline");
+    const uint32_t tmem = gemm_setup<GeomSmall>(s, maps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = a.route.T;
@@ -122,11 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* soff = cnt + MM_MAX_EXPERTS;                        // [P+1]
     int* stoff = soff + MM_MAX_EXPERTS + 1;                  // [P]
     const int chunk = ((N + kSmallWarps - 1) / kSmallWarps + 31) & ~31;
+    bool short_tiles = true;
     const int lo = min(N, warp * chunk), hi = min(N, lo + chunk);
     const uint32_t lt = (1u << lane) - 1u;
     if (ok) {
         for (int i = threadIdx.x; i < N; i += kThreads) sphys[i] = a.route.phys[i];
         for (int i = threadIdx.x; i < kSmallWarps * P; i += kThreads) wcnt[(i / P) * MM_MAX_EXPERTS + i % P] = 0;
+        if (threadIdx.x < 2) scal[2 + threadIdx.x] = 0;
         __syncthreads();
         int* wc = wcnt + warp * MM_MAX_EXPERTS;
         for (int base = lo; base < hi; base += 32) {
@@ -145,8 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 run += v;
             }
             cnt[p] = run;
+            if (run > 0) {
+                atomicAdd(&scal[2], tiles_of(run, kSmallTile));
+                atomicAdd(&scal[3], tiles_of(run, kTokTile));
+            }
         }
         __syncthreads();
+        // short tiles unless they would add more than 1/16 to the tile count
+        short_tiles = 16 * scal[2] <= 17 * scal[3];
+        const int tile = short_tiles ? kSmallTile : kTokTile;
         if (warp == 0) {
             // exclusive scans over experts of the padded segment sizes and tile counts
             const int per = (P + 31) / 32;
@@ -154,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int rows = 0, tiles = 0;
             for (int p = p0; p < p1; ++p) {
                 rows += seg_rows(cnt[p]);
-                tiles += tiles_of(cnt[p]);
+                tiles += tiles_of(cnt[p], tile);
             }
             int rx = rows, tx = tiles;
 #pragma unroll
@@ -171,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 soff[p] = ro;
                 stoff[p] = to;
                 ro += seg_rows(cnt[p]);
-                to += tiles_of(cnt[p]);
+                to += tiles_of(cnt[p], tile);
             }
             if (lane == 31) {
                 soff[P] = rx;
@@ -181,11 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         for (int p = threadIdx.x; p < P; p += kThreads) {
-            const int nt = tiles_of(cnt[p]);
+            const int nt = tiles_of(cnt[p], tile);
             for (int t = 0; t < nt; ++t) {
                 t_expert[stoff[p] + t] = p;
-                t_row0[stoff[p] + t] = soff[p] + t * kTokTile;
-                t_rows[stoff[p] + t] = min(kTokTile, cnt[p] - t * kTokTile);
+                t_row0[stoff[p] + t] = soff[p] + t * tile;
+                t_rows[stoff[p] + t] = min(tile, cnt[p] - t * tile);
             }
         }
         for (int base = lo; base < hi; base += 32) {
@@ -220,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
              it += static_cast<int64_t>(gridDim.x) * kThreads) {
             const int64_t t = it / nb;
             quant_dispatch_block(a.x, t, static_cast<int>(it % nb), H, k, spos + t * k, sphys + t * k, soff, stoff,
-                                 a.xq, a.xs_t);
+                                 tile, a.xq, a.xs_t);
         }
         fence_proxy_async_global();
     }
@@ -236,7 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tv.row0 = t_row0;
         tv.rows = t_rows;
         tv.ntiles = scal[0];
-        gemm_roles(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+        if (short_tiles)
+            gemm_roles<GeomSmall>(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+        else
+            gemm_roles<GeomLarge>(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
     }
     gemm_teardown(tmem);
     if (threadIdx.x == 0) stamp[5] = globaltimer();

@@ -149,7 +149,7 @@ __device__ __forceinline__ void route_token_any(const RouteArgs& a, int64_t t, i
 // scale tile of the row's token tile.
 __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
                                                      int k, const int32_t* pos_t, const int32_t* phys_t,
-                                                     const int32_t* off, const int32_t* toff,
+                                                     const int32_t* off, const int32_t* toff, int tile,
                                                      uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t)
 {
     const uint4* src = reinterpret_cast<const uint4*>(x + t * H + b * 32);
@@ -188,7 +188,7 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         const int p = phys_t[j];
         const int rank = static_cast<int>(row) - off[p];
-        xs_t[act_sf_offset(toff[p] + rank / kTokTile, rank % kTokTile, b, kchunks)] = sbyte;
+        xs_t[act_sf_offset(toff[p] + rank / tile, rank % tile, b, kchunks)] = sbyte;
     }
 }
 

@@ -229,3 +229,42 @@ def test_rebalance_keeps_outputs_and_spreads_load(torch, T):
     assert load2.max() < load1.max()
     pol, rc = oracle.plan_replicas(counts, cfg.P, 4)
     assert np.array_equal(r2["phys"], oracle.eplb(r2["idx"], pol, rc))
+
+
+def _check_tiles(res, P, tile):
+    """Token tiles cut each expert's segment into consecutive `tile`-row pieces."""
+    tiles = res["tiles"].reshape(-1, 3)
+    off = res["offsets"]
+    count = np.bincount(res["phys"].ravel(), minlength=P)
+    want = []
+    for p in range(P):
+        for j in range((count[p] + tile - 1) // tile):
+            want.append((p, off[p] + j * tile, min(tile, count[p] - j * tile)))
+    assert tiles.tolist() == [list(w) for w in want]
+
+
+@pytest.mark.parametrize("case", ["short", "full_small", "large"])
+def test_tile_table_and_tile_size_choice(torch, case):
+    # short: one hot expert of 100 rows among many small ones; 64-row tiles add
+    # one tile in 33, so the fused kernel takes them.  full_small: eight
+    # experts of 512 rows; 64-row tiles would double the tiles, so it takes
+    # 128.  large: the large-input path always cuts 128-row tiles.
+    T = {"short": 200, "full_small": 512, "large": 1100}[case]
+    k = 2 if case == "short" else 8
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T, H=256, I=128, E=32, P=32, k=k)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    if case == "short":
+        logits[:100, 0] += 20.0
+    elif case == "full_small":
+        logits[:, :8] += 20.0
+    W = synthetic.make_all_weights(cfg)
+    run = gpu_util.Run(cfg, W, cap=T)
+    res = run.forward(hidden, logits, bias)
+    route = run.op.last_info()[0]
+    run.close()
+    assert res["status"] == 0
+    assert route == (2 if case == "large" else 1)
+    if case == "short":
+        assert np.bincount(res["phys"].ravel(), minlength=cfg.P)[0] > 64
+    _check_tiles(res, cfg.P, 64 if case == "short" else 128)
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(T, 32))
