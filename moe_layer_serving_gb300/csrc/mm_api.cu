@@ -386,7 +386,7 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     add(chunks * c->P * 4);
     add((c->P + 1) * 4);
     add(c->P * 4);                            // first tile of each expert
-    add(tiles * 4 * 4 + 4);                   // tile table, done1, num_tiles
+    add(tiles * 4 * 4 + 8);                   // tile table, done1, num_tiles, unit counter
     add(rows * H);
     add(tiles * (H / 128) * 512);
     add(rows * I);
@@ -415,7 +415,8 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->tile_row0 = carve<int32_t>(p, tiles);
     c->tile_rows = carve<int32_t>(p, tiles);
     c->done1 = carve<int32_t>(p, tiles);
-    c->num_tiles = carve<int32_t>(p, 1);
+    c->num_tiles = carve<int32_t>(p, 2);
+    c->unit_next = c->num_tiles + 1;
     c->xq = carve<uint8_t>(p, rows * H);
     c->xs_t = carve<uint8_t>(p, tiles * (H / 128) * 512);
     c->hq = carve<uint8_t>(p, rows * I);

@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tv.row0 = g.tile_row0;
     tv.rows = g.tile_rows;
     tv.ntiles = *g.num_tiles;
-    gemm_roles<Geo>(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+    gemm_roles<Geo>(maps, g, tv, s, tmem);
     gemm_teardown(tmem);
 }
 
@@ -53,6 +53,7 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.tile_rows = c->tile_rows;
     g.num_tiles = c->num_tiles;
     g.done1 = c->done1;
+    g.unit_next = c->unit_next;
     g.status = c->status;
     g.H = c->H;
     g.I = c->I;

@@ -18,9 +18,13 @@
 //   GEMM2 unit (tile, m-block mb): B = W2[p] rows [mb*256, +256); the
 //       epilogue writes y rows in bf16.
 //
-// A persistent CTA walks units u = first, first + stride, ...; all GEMM1 units
-// precede all GEMM2 units, and a GEMM2 unit waits (bounded) until the GEMM1
-// units of its tile have published hq.  Warp roles: 0 = TMA producer, 1 =
+// Units are handed out at run time: the producer thread of a CTA takes the
+// next unit number from a global counter and passes it to the CTA's MMA and
+// epilogue warps through a small ring in shared memory, so CTAs that drew
+// cheaper units take more of them (GEMM1 units stream 3.5x the weight bytes of
+// GEMM2 units, so a fixed round-robin split leaves some SMs a whole GEMM1 unit
+// behind).  All GEMM1 units precede all GEMM2 units, and a GEMM2 unit waits
+// (bounded) until the GEMM1 units of its tile have published hq.  Warp roles: 0 = TMA producer, 1 =
 // tensor-memory owner + MMA issuer, 2..9 = epilogue.  The eight epilogue warps
 // first drain the accumulator into registers (each warp: its 32 token rows,
 // half of the columns) and release tensor memory, so the next unit's MMAs run
@@ -132,17 +136,21 @@ __device__ __forceinline__ int ld_acquire(const int* p)
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // shared-memory carve-up of the GEMM machinery (base aligned to 1024 bytes)
+constexpr int kURing = 4;                // units queued ahead in shared memory
 struct GemmSmem {
     uint8_t* stages;
     uint64_t* full;
     uint64_t* empty;
     uint64_t* tmem_full;
     uint64_t* tmem_empty;
+    uint64_t* ufull;          // [kURing] unit slot written (producer)
+    uint64_t* uempty;         // [kURing] unit slot read (MMA thread + every epilogue thread)
     uint32_t* tmem_slot;
     volatile int* abort_flag;
+    volatile int* uring;      // [kURing] unit numbers
 };
-// Barrier block (256 bytes): full[8], empty[8], tmem_full, tmem_empty, the
-// TMEM base and the abort flag.  Its layout does not depend on the stage
+// Barrier block (256 bytes): full[8], empty[8], tmem_full, tmem_empty,
+// ufull[4], uempty[4], the TMEM base, the abort flag and the unit ring.  Its layout does not depend on the stage
 // count, so one kernel can run either geometry over the same buffers.
 constexpr int kMaxStages = 8;
 __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
@@ -153,8 +161,12 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
     s.empty = s.full + kMaxStages;
     s.tmem_full = s.empty + kMaxStages;
     s.tmem_empty = s.tmem_full + 1;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.tmem_empty + 1);
+    s.ufull = s.tmem_empty + 1;
+    s.uempty = s.ufull + kURing;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.uempty + kURing);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+    s.uring = s.abort_flag + 1;
+    static_assert((2 * kMaxStages + 2 + 2 * kURing) * 8 + 8 + 4 * kURing <= 256, "barrier block");
     return s;
 }
 
@@ -170,6 +182,10 @@ __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps
         }
         mbar_init(s.tmem_full, 1);
         mbar_init(s.tmem_empty, kEpiThreads);
+        for (int i = 0; i < kURing; ++i) {
+            mbar_init(&s.ufull[i], 1);
+            mbar_init(&s.uempty[i], 1 + kEpiThreads);
+        }
         *s.abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&maps.w1);
@@ -197,10 +213,44 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem)
     }
 }
 
+// ---- unit queue ----------------------------------------------------------------
+struct UnitQueue {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance()
+    {
+        if (++slot == kURing) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Producer: take the next unit number and queue it for the CTA's consumers.
+__device__ __forceinline__ bool push_unit(const GemmArgs& g, const GemmSmem& s, UnitQueue& q, int& u)
+{
+    u = *s.abort_flag ? 0x7FFFFFFF : atomicAdd(g.unit_next, 1);
+    if (!mbar_wait(&s.uempty[q.slot], q.phase ^ 1u, g.status, s.abort_flag, kSiteUnitQueue)) return false;
+    s.uring[q.slot] = u;
+    mbar_arrive(&s.ufull[q.slot]);
+    q.advance();
+    return true;
+}
+
+// MMA thread / epilogue thread: the next unit the producer queued.
+__device__ __forceinline__ bool pop_unit(const GemmArgs& g, const GemmSmem& s, UnitQueue& q, int& u)
+{
+    if (!mbar_wait(&s.ufull[q.slot], q.phase, g.status, s.abort_flag, kSiteUnitQueue)) return false;
+    u = s.uring[q.slot];
+    mbar_arrive(&s.uempty[q.slot]);
+    q.advance();
+    return true;
+}
+
 // ---- producer: one thread issues every TMA / bulk copy -----------------------
 template <class G>
 __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
-                                              const GemmSmem& s, int first_unit, int unit_stride)
+                                              const GemmSmem& s)
 {
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
@@ -210,7 +260,10 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
     int armed[kStages];
     for (int i = 0; i < kStages; ++i) armed[i] = -1;
     Unit un;
-    for (int u = first_unit; decode_unit(g, tv, u, un) && !*s.abort_flag; u += unit_stride) {
+    UnitQueue q;
+    for (;;) {
+        int u;
+        if (!push_unit(g, s, q, u) || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
         const CUtensorMap* wmap = un.phase == 1 ? &maps.w1 : (un.nw == 2 ? &maps.w2 : &maps.w2_one);
         const CUtensorMap* amap = un.phase == 1 ? &maps.xq[un.tbox] : &maps.hq[un.tbox];
         const uint8_t* wsf = un.phase == 1 ? g.w1_sf : g.w2_sf;
@@ -276,8 +329,7 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
 // the add never carries out of that field).  The instruction descriptors of a
 // unit are formed once per unit.
 template <class G>
-__device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, const GemmSmem& s, uint32_t tmem,
-                                         int first_unit, int unit_stride)
+__device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, const GemmSmem& s, uint32_t tmem)
 {
     const uint64_t a_desc0 = desc_kmajor_sw128(s.stages);
     const uint64_t b_desc0 = desc_kmajor_sw128(s.stages + G::kABytes);
@@ -290,7 +342,10 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, 
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     Unit un;
-    for (int u = first_unit; decode_unit(g, tv, u, un) && !*s.abort_flag; u += unit_stride) {
+    UnitQueue q;
+    for (;;) {
+        int u;
+        if (!pop_unit(g, s, q, u) || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
         if (!mbar_wait(s.tmem_empty, acc_phase ^ 1u, g.status, s.abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
         const uint32_t n = static_cast<uint32_t>(un.nw * kTile);
@@ -344,7 +399,7 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16])
 // Warp w reads TMEM lanes 32*(w % 4) .. +32 (token rows) and column half
 // (w - 2) / 4 of the unit's columns.
 __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView& tv, const GemmSmem& s,
-                                              uint32_t tmem, int first_unit, int unit_stride)
+                                              uint32_t tmem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;                       // TMEM lane quarter
@@ -353,7 +408,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView&
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
     uint32_t acc_phase = 0;
     Unit un;
-    for (int u = first_unit; decode_unit(g, tv, u, un) && !*s.abort_flag; u += unit_stride) {
+    UnitQueue uq;
+    for (;;) {
+        int u;
+        if (!pop_unit(g, s, uq, u) || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
         if (!mbar_wait(s.tmem_full, acc_phase, g.status, s.abort_flag, kSiteEpiTmemFull)) break;
         tc_fence_after();
         const bool active = 32 * q < un.rows;                       // warp-uniform
@@ -447,18 +505,18 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView&
     }
 }
 
-// All threads: each warp runs its role over units first_unit, +unit_stride, ...
+// All threads: each warp runs its role over the units the CTA's producer draws.
 template <class G>
 __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
-                                           const GemmSmem& s, uint32_t tmem, int first_unit, int unit_stride)
+                                           const GemmSmem& s, uint32_t tmem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 0) {
-        if (lane == 0) producer_loop<G>(maps, g, tv, s, first_unit, unit_stride);
+        if (lane == 0) producer_loop<G>(maps, g, tv, s);
     } else if (warp == 1) {
-        if (lane == 0) mma_loop<G>(g, tv, s, tmem, first_unit, unit_stride);
+        if (lane == 0) mma_loop<G>(g, tv, s, tmem);
     } else {
-        epilogue_loop(g, tv, s, tmem, first_unit, unit_stride);
+        epilogue_loop(g, tv, s, tmem);
     }
 }
 

@@ -132,6 +132,7 @@ struct GemmArgs {
     const int* tile_rows;
     const int* num_tiles;
     int* done1;             // per token tile: GEMM1 units finished
+    int* unit_next;         // next unit to hand out (zeroed before the GEMM phase)
     int* status;
     int H, I, P;
     int phases;             // bit 0: GEMM1 units, bit 1: GEMM2 units
@@ -164,6 +165,7 @@ struct mm_ctx {
     float* wgt = nullptr;
     int32_t *chunk_hist = nullptr, *off = nullptr, *toff = nullptr, *tile_expert = nullptr, *tile_row0 = nullptr,
             *tile_rows = nullptr, *num_tiles = nullptr, *done1 = nullptr;
+    int32_t* unit_next = nullptr;   // the GEMM kernels' unit counter (num_tiles[1])
     uint8_t *xq = nullptr, *xs_t = nullptr, *hq = nullptr, *hs_t = nullptr;
     __nv_bfloat16* y = nullptr;
     int* status = nullptr;
@@ -190,6 +192,7 @@ enum WaitSite {
     kSiteEpiTmemFull = 4,
     kSiteProducerDone1 = 5,
     kSiteGridBarrier = 6,
+    kSiteUnitQueue = 7,
 };
 
 // Fault injection for the failure-detection tests (environment variable

@@ -86,7 +86,7 @@ struct ScanArgs {
     int32_t* tile_expert;
     int32_t* tile_row0;
     int32_t* tile_rows;
-    int32_t* num_tiles;
+    int32_t* num_tiles;    // [0] tiles; [1] the GEMM kernel's unit counter, reset here
     int32_t* done1;
 };
 
@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
         }
         if (p == a.P - 1) {
             a.off[a.P] = off_incl;
-            *a.num_tiles = tiles_incl;
+            a.num_tiles[0] = tiles_incl;
+            a.num_tiles[1] = 0;
         }
     }
 }

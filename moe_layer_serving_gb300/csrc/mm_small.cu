@@ -228,7 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 a.tile_rows[t] = t_rows[t];
                 g.done1[t] = 0;
             }
-            if (threadIdx.x == 0) *a.num_tiles = scal[0];
+            if (threadIdx.x == 0) {
+                a.num_tiles[0] = scal[0];
+                a.num_tiles[1] = 0;     // the GEMM phase's unit counter
+            }
         }
 
         // ---- D: MXFP8 quantisation + dispatch ------------------------------
@@ -254,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tv.rows = t_rows;
         tv.ntiles = scal[0];
         if (short_tiles)
-            gemm_roles<GeomSmall>(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+            gemm_roles<GeomSmall>(maps, g, tv, s, tmem);
         else
-            gemm_roles<GeomLarge>(maps, g, tv, s, tmem, blockIdx.x, gridDim.x);
+            gemm_roles<GeomLarge>(maps, g, tv, s, tmem);
     }
     gemm_teardown(tmem);
     if (threadIdx.x == 0) stamp[5] = globaltimer();

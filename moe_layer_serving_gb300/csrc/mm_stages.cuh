@@ -64,57 +64,71 @@ struct RouteArgs {
     int E, k, R;
 };
 
-// One warp routes token t: lane l holds experts l, l+32, ...; k rounds of a
-// warp arg-max over (key, -expert) select the experts in order, ties to the
-// lower expert index.  Lane 0 writes idx/w/phys and counts the selections:
-// into shared memory (hist != null) or straight into the global table.
+// Order-preserving map of a binary32 key to uint32 (larger key, larger code).
+// Routing keys are sigmoid scores plus a finite bias: never NaN or -0, so
+// equal codes are exactly equal keys.
+__device__ __forceinline__ uint32_t key_code(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp routes token t: lane l holds experts l, l+32, ...  Each lane keeps
+// the best of its own remaining experts; a round takes the warp maximum of
+// those keys and, among the lanes that hold it, the lowest expert index (ties
+// go to the lower expert), so k rounds select the experts in order.  Lane j
+// keeps the j-th selection; lanes 0..k-1 write idx/w/phys and count the
+// selections into shared memory (hist != null) or the global table.
 template <int VPL>
 __device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int lane, int* hist)
 {
-    float s[VPL], key[VPL];
+    float s[VPL];
+    uint32_t code[VPL];
     uint32_t avail = 0;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
         s[i] = 0.0f;
-        key[i] = 0.0f;
+        code[i] = 0u;
         if (e < a.E) {
             s[i] = sigmoid_spec(a.logits[t * a.E + e]);
-            key[i] = __fadd_rn(s[i], a.bias ? a.bias[e] : 0.0f);
+            code[i] = key_code(__fadd_rn(s[i], a.bias ? a.bias[e] : 0.0f));
             avail |= 1u << i;
         }
     }
-    // lane j keeps the j-th selection
+    // this lane's best remaining expert: code, slot i, score
+    uint32_t lc = 0u;
+    int li = -1;
+    float ls = 0.0f;
+    auto local_best = [&]() {
+        lc = 0u;
+        li = -1;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            if (((avail >> i) & 1u) && (li < 0 || code[i] > lc)) {
+                lc = code[i];
+                li = i;
+                ls = s[i];
+            }
+        }
+    };
+    local_best();
     int my_e = 0;
     float my_s = 0.0f;
 #pragma unroll
     for (int j = 0; j < MM_MAX_TOPK; ++j) {
         if (j >= a.k) break;
-        float bk = -INFINITY, bs = 0.0f;
-        int be = 0x7FFFFFFF;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            if (((avail >> i) & 1u) && (be == 0x7FFFFFFF || key[i] > bk)) {
-                bk = key[i];
-                bs = s[i];
-                be = lane + 32 * i;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
-            const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
-            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-            if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ok > bk || (ok == bk && oe < be))) {
-                bk = ok;
-                bs = os;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, li >= 0 ? lc : 0u);
+        const uint32_t cand = (li >= 0 && lc == m) ? static_cast<uint32_t>(lane + 32 * li) : 0xFFFFFFFFu;
+        const int be = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
+        const float bs = __shfl_sync(0xFFFFFFFFu, ls, be & 31);
         if (lane == j) {
             my_e = be;
             my_s = bs;
+        }
+        if ((be & 31) == lane) {
+            avail &= ~(1u << (be >> 5));
+            local_best();
         }
     }
     // sum of the selected scores in selection order (the same in every lane)
@@ -193,22 +207,34 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
 }
 
 // out[t][8c .. 8c+8) = bf16( sum_j w[t,j] * y[pos[t,j]][...] ), fp32, j in order.
+// All k row loads are issued before the sum starts, so one thread keeps k
+// 16-byte reads in flight instead of one.
 __device__ __forceinline__ void combine_chunk(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w,
                                               const int32_t* __restrict__ pos, int64_t t, int c, int H, int k,
                                               __nv_bfloat16* __restrict__ out)
 {
+    float wj[MM_MAX_TOPK];
+    uint4 u[MM_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MM_MAX_TOPK; ++j) {
+        if (j < k) {
+            wj[j] = w[t * k + j];
+            const int64_t row = pos[t * k + j];
+            u[j] = *(reinterpret_cast<const uint4*>(y + row * H) + c);
+        }
+    }
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-        const float wj = w[t * k + j];
-        const int64_t row = pos[t * k + j];
-        const uint4 u = *(reinterpret_cast<const uint4*>(y + row * H) + c);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(wj, __uint_as_float(w4[i] << 16), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(wj, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    for (int j = 0; j < MM_MAX_TOPK; ++j) {
+        if (j < k) {
+            const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj[j], __uint_as_float(w4[i] << 16), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj[j], __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+            }
         }
     }
     uint32_t o[4];
