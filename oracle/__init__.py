@@ -1,4 +1,5 @@
-"""CPU oracle for the a8w4 fused MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the fused MoE layer forward (a8w4, and the a16w4 variant) --
+TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (``moe_layer_serving_gb300``)
@@ -51,6 +52,8 @@ def lib():
             "orc_expert_down": (None, [i64, i32, i32, p, p, p, p, p]),
             "orc_expert_ffn": (None, [i64, i32, i32, p, p, p, p, p, p, p, p, p, p, p]),
             "orc_combine": (None, [i64, i32, i32, p, p, p]),
+            "orc_expert_down_a16": (None, [i64, i32, i32, p, p, p, p]),
+            "orc_expert_ffn_a16": (None, [i64, i32, i32, p, p, p, p, p, p, p, p, p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -189,6 +192,35 @@ def expert_ffn(xq, xs, w1, w1s, w2, w2s, want_g=False):
     return out
 
 
+def expert_down_a16(hb, w2, w2s):
+    """bf16 bits hb [rows,I] -> y float32 [rows,H] (fp64 sums rounded to fp32)"""
+    hb = _c(hb, np.uint16)
+    w2, w2s = _c(w2, np.uint8), _c(w2s, np.uint8)
+    rows, I = hb.shape
+    H = w2.shape[0]
+    y = np.empty((rows, H), np.float32)
+    lib().orc_expert_down_a16(rows, H, I, _ptr(hb), _ptr(w2), _ptr(w2s), _ptr(y))
+    return y
+
+
+def expert_ffn_a16(x, w1, w1s, w2, w2s, want_g=False):
+    """One expert on bf16 rows x [rows,H] (bits) -> dict(hb, h, y[, g])."""
+    x = _c(x, np.uint16)
+    w1, w1s, w2, w2s = (_c(a, np.uint8) for a in (w1, w1s, w2, w2s))
+    rows, H = x.shape
+    I = w2.shape[1] * 2
+    hb = np.empty((rows, I), np.uint16)
+    h = np.empty((rows, I), np.float32)
+    g = np.empty((rows, 2 * I), np.float32) if want_g else None
+    y = np.empty((rows, H), np.float32)
+    lib().orc_expert_ffn_a16(rows, H, I, _ptr(x), _ptr(w1), _ptr(w1s), _ptr(w2), _ptr(w2s),
+                             _ptr(hb), _ptr(g), _ptr(h), _ptr(y))
+    out = dict(hb=hb, h=h, y=y)
+    if want_g:
+        out["g"] = g
+    return out
+
+
 def combine(w, ypair):
     """w [T,k] f32, ypair [T*k, H] f32 in pair order -> bf16 bits [T,H]"""
     w = _c(w, np.float32)
@@ -201,14 +233,20 @@ def combine(w, ypair):
 
 
 def forward(hidden, logits, bias, k, weights, phys_of_logical=None, replica_counts=None,
-            token_ids=None, want_g=False):
+            token_ids=None, want_g=False, act="mxfp8"):
     """The whole layer for the given tokens.
 
     hidden bf16 bits [n,H], logits [n,E] for tokens ``token_ids`` (their index
     in the forward call; default 0..n-1).  weights = (w1, w1s, w2, w2s) indexed
-    by physical expert.  Returns a dict of every intermediate (pair order is
-    (token, slot)) plus ``out`` (bf16 bits [n,H]) and ``counts`` (int64 [E]).
+    by physical expert.  ``act``: "mxfp8" (a8w4: activations quantised to
+    MXFP8 before each GEMM) or "bf16" (a16w4: bf16 activations, h rounded to
+    bf16).  Returns a dict of every intermediate (pair order is (token, slot))
+    plus ``out`` (bf16 bits [n,H]) and ``counts`` (int64 [E]).
     """
+    if act == "bf16":
+        return _forward_a16(hidden, logits, bias, k, weights, phys_of_logical, replica_counts,
+                            token_ids, want_g)
+    assert act == "mxfp8", act
     w1, w1s, w2, w2s = weights
     n, H = hidden.shape
     E = logits.shape[1]
@@ -240,6 +278,41 @@ def forward(hidden, logits, bias, k, weights, phys_of_logical=None, replica_coun
     out = combine(w, ypair)
     res = dict(idx=idx, w=w, phys=phys, counts=counts, xq=xq, xs=xs, offsets=off,
                order=order, pos=pos, hq=hq, hs=hs, h=h, y=ypair, out=out)
+    if want_g:
+        res["g"] = g
+    return res
+
+
+def _forward_a16(hidden, logits, bias, k, weights, phys_of_logical, replica_counts, token_ids,
+                 want_g):
+    w1, w1s, w2, w2s = weights
+    n, H = hidden.shape
+    E = logits.shape[1]
+    P = w1.shape[0]
+    if phys_of_logical is None:
+        phys_of_logical = np.arange(E, dtype=np.int32)[:, None]
+        replica_counts = np.ones(E, np.int32)
+    idx, w = route(logits, bias, k)
+    phys = eplb(idx, phys_of_logical, replica_counts, token_ids)
+    counts = record(idx, E)
+    off, order, pos = permute(phys, P)
+    I = w2.shape[2] * 2
+    npairs = n * k
+    hb = np.zeros((npairs, I), np.uint16)
+    h = np.zeros((npairs, I), np.float32)
+    g = np.zeros((npairs, 2 * I), np.float32) if want_g else None
+    ypair = np.zeros((npairs, H), np.float32)
+    for p in range(P):
+        pairs = order[off[p]:off[p + 1]]
+        if pairs.size == 0:
+            continue
+        r = expert_ffn_a16(hidden[pairs // k], w1[p], w1s[p], w2[p], w2s[p], want_g=want_g)
+        hb[pairs], h[pairs], ypair[pairs] = r["hb"], r["h"], r["y"]
+        if want_g:
+            g[pairs] = r["g"]
+    out = combine(w, ypair)
+    res = dict(idx=idx, w=w, phys=phys, counts=counts, offsets=off, order=order, pos=pos,
+               hb=hb, h=h, y=ypair, out=out)
     if want_g:
         res["g"] = g
     return res

@@ -25,6 +25,12 @@
  *   combine  out[t] = bf16(sum_j w[t,j] * y[t,j]) in fp64, rounded to fp32
  *            then to bf16 (nearest-even)
  *
+ * The a16w4 variant (bf16 activations with the same MXFP4 experts, the other
+ * serving arms of "InferenceX PR #3430", draft-precision notes) skips the
+ * activation quantisation: GEMM1 reads the bf16 hidden rows, h is rounded to
+ * bf16 (the activation type of that arm) and GEMM2 reads it; routing,
+ * dispatch and combine are the same.
+ *
  * Where the pages are silent the plainest reading is taken; every such
  * reading is spelled out beside the function that makes it.
  *
@@ -276,6 +282,16 @@ void orc_permute(int64_t npairs, int P, const int32_t *phys, int64_t *offsets,
     free(fill);
 }
 
+static uint16_t bf16_rne(float f)
+{
+    uint32_t b = bits_from_f32(f);
+    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x7FFFFFu)) return (uint16_t)((b >> 16) | 0x40);
+    b += 0x7FFFu + ((b >> 16) & 1u);
+    return (uint16_t)(b >> 16);
+}
+
+static double bf16_value(uint16_t h) { return (double)f32_from_bits((uint32_t)h << 16); }
+
 /* one row of an MXFP4 matrix (K values) as exact doubles */
 static void mxfp4_row(int K, const uint8_t *packed, const uint8_t *scale, double *out)
 {
@@ -355,13 +371,6 @@ void orc_expert_ffn(int64_t rows, int H, int I, const uint8_t *xq, const uint8_t
     orc_expert_down(rows, H, I, hq, hs, w2, w2s, y);
 }
 
-static uint16_t bf16_rne(float f)
-{
-    uint32_t b = bits_from_f32(f);
-    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x7FFFFFu)) return (uint16_t)((b >> 16) | 0x40);
-    b += 0x7FFFu + ((b >> 16) & 1u);
-    return (uint16_t)(b >> 16);
-}
 
 /* combine: ypair[(t*k + j)*H + m] is y of pair (t, j).  Reading: the top-k
  * weight is applied here, not inside GEMM2. */
@@ -375,4 +384,68 @@ void orc_combine(int64_t T, int k, int H, const float *w, const float *ypair, ui
                 acc += (double)w[t * k + j] * (double)ypair[(t * k + j) * H + m];
             out[t * H + m] = bf16_rne((float)acc);
         }
+}
+
+/* ---- a16w4: bf16 activations x MXFP4 experts ---------------------------- */
+
+/* GEMM2 for rows of one expert, bf16 input: y[r][m] = sum_i hb[r][i] * W2[m][i]
+ * (fp64 accumulation of exact products, rounded to fp32). */
+void orc_expert_down_a16(int64_t rows, int H, int I, const uint16_t *hb, const uint8_t *w2,
+                         const uint8_t *w2s, float *y)
+{
+    double *a = (double *)malloc(sizeof(double) * rows * I);
+    for (int64_t j = 0; j < rows * I; ++j) a[j] = bf16_value(hb[j]);
+#pragma omp parallel
+    {
+        double *wrow = (double *)malloc(sizeof(double) * I);
+#pragma omp for schedule(static)
+        for (int m = 0; m < H; ++m) {
+            mxfp4_row(I, w2 + (int64_t)m * (I / 2), w2s + (int64_t)m * (I / 32), wrow);
+            for (int64_t r = 0; r < rows; ++r) {
+                double acc = 0.0;
+                for (int i = 0; i < I; ++i) acc += a[r * I + i] * wrow[i];
+                y[r * H + m] = (float)acc;
+            }
+        }
+        free(wrow);
+    }
+    free(a);
+}
+
+/* GEMM1 + SwiGLU + GEMM2 for rows of one expert with bf16 activations x.
+ * G = x . W1^T (fp64, rounded to fp32); gate = G[:, :I], up = G[:, I:];
+ * h = silu(gate) * up formed from the fp32 G, rounded to fp32 and then to
+ * bf16 (nearest-even): hb is GEMM2's input.  g_out [rows,2I] and h_out
+ * [rows,I] (h before the bf16 rounding) are optional. */
+void orc_expert_ffn_a16(int64_t rows, int H, int I, const uint16_t *x, const uint8_t *w1,
+                        const uint8_t *w1s, const uint8_t *w2, const uint8_t *w2s, uint16_t *hb,
+                        float *g_out, float *h_out, float *y)
+{
+    double *a = (double *)malloc(sizeof(double) * rows * H);
+    float *G = (float *)malloc(sizeof(float) * rows * 2 * I);
+    for (int64_t j = 0; j < rows * H; ++j) a[j] = bf16_value(x[j]);
+#pragma omp parallel
+    {
+        double *wrow = (double *)malloc(sizeof(double) * H);
+#pragma omp for schedule(static)
+        for (int n = 0; n < 2 * I; ++n) {
+            mxfp4_row(H, w1 + (int64_t)n * (H / 2), w1s + (int64_t)n * (H / 32), wrow);
+            for (int64_t r = 0; r < rows; ++r) {
+                double acc = 0.0;
+                for (int k = 0; k < H; ++k) acc += a[r * H + k] * wrow[k];
+                G[r * 2 * I + n] = (float)acc;
+            }
+        }
+        free(wrow);
+    }
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < I; ++i) {
+            double g = G[r * 2 * I + i], u = G[r * 2 * I + I + i];
+            float h = (float)(g / (1.0 + exp(-g)) * u);
+            if (h_out) h_out[r * I + i] = h;
+            hb[r * I + i] = bf16_rne(h);
+        }
+    if (g_out) memcpy(g_out, G, sizeof(float) * rows * 2 * I);
+    free(a); free(G);
+    orc_expert_down_a16(rows, H, I, hb, w2, w2s, y);
 }
