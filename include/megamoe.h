@@ -70,6 +70,11 @@ typedef enum {
     MM_ROUTE_LARGE = 2  /* always the large path */
 } mm_route;
 
+typedef enum {
+    MM_ACT_MXFP8 = 0,   /* a8w4: activations quantised to MXFP8 before each expert GEMM (default) */
+    MM_ACT_BF16 = 1     /* a16w4: bf16 activations into both expert GEMMs, h rounded to bf16 */
+} mm_act;
+
 #define MM_MAX_LAYERS 256
 #define MM_MAX_EXPERTS 512
 #define MM_MAX_TOPK 8
@@ -125,6 +130,20 @@ MM_API mm_status mm_set_recording(mm_handle h, int on);
  * set_large_m_enabled, "sglang PR #47065", aiter commit message). */
 MM_API mm_status mm_set_route(mm_handle h, mm_route route);
 
+/* Activation format of later forwards.  MM_ACT_MXFP8 is the fused a8w4
+ * operator ("sglang PR #47065"; "InferenceX PR #3430", draft-precision notes:
+ * the expert-parallel arm runs MegaMoE a8w4 on the MXFP4 experts).
+ * MM_ACT_BF16 is the a16w4 variant of the other serving arms (same notes:
+ * MXFP4 experts with the default bf16 activations): the hidden rows are
+ * dispatched in bf16, GEMM1 runs bf16 x MXFP4 with fp32 accumulation,
+ * h = silu(gate) * up is rounded to bf16 and GEMM2 runs bf16 x MXFP4; routing,
+ * EPLB remap, recording and combine are unchanged.  The bf16 format runs the
+ * multi-launch path only: with it, mm_set_route(MM_ROUTE_SMALL) makes
+ * mm_forward return MM_ERR_UNSUPPORTED.  Changing the format drops the
+ * workspace (call mm_reserve again before forwarding).  Synchronous; not
+ * allowed during stream capture.  An unknown value -> MM_ERR_INVALID_ARG. */
+MM_API mm_status mm_set_activation_format(mm_handle h, mm_act act);
+
 /* Reserve workspace for up to max_tokens tokens per forward (the pages' MTPR
  * capacity).  Allocates; call before any stream capture.  Calling again with
  * a larger value reallocates (synchronous); a smaller value is a no-op. */
@@ -165,9 +184,11 @@ MM_API mm_status mm_get_status(mm_handle h, int *device_code);
  *   4 offsets int32 [P + 1]    start row of each physical expert's segment
  *                              (segments are padded to 16 rows); [P] = total
  *   5 xq      uint8 [rows, H]  dispatched MXFP8 activation codes
- *   6 xs      uint8 [rows, H/32] their scale bytes, row-major
+ *             (bf16 format: the dispatched bf16 rows [rows, H])
+ *   6 xs      uint8 [rows, H/32] their scale bytes, row-major (bf16: empty)
  *   7 hq      uint8 [rows, I]  GEMM1 output codes (after SwiGLU, requant)
- *   8 hs      uint8 [rows, I/32] their scale bytes, row-major
+ *             (bf16 format: h in bf16 [rows, I])
+ *   8 hs      uint8 [rows, I/32] their scale bytes, row-major (bf16: empty)
  *   9 y       bf16  [rows, H]  GEMM2 output rows
  * where rows = offsets[P].  Copies min(bytes, size of the stage) bytes into
  * dst_host; MM_ERR_INVALID_ARG for an unknown stage. */

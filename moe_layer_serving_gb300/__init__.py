@@ -14,7 +14,7 @@ import os
 import numpy as np
 
 __all__ = ["lib", "MegaMoE", "MegaMoEError", "library_path", "STATUS", "ROUTE_AUTO", "ROUTE_SMALL",
-           "ROUTE_LARGE", "DUMP_STAGES"]
+           "ROUTE_LARGE", "ACT_MXFP8", "ACT_BF16", "DUMP_STAGES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libmegamoe.so")
@@ -24,6 +24,7 @@ STATUS = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_E
 MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_NOT_READY = 0, 1, 2, 3
 MM_ERR_CAPACITY, MM_ERR_CUDA, MM_ERR_TIMEOUT, MM_ERR_DEVICE = 4, 5, 6, 7
 ROUTE_AUTO, ROUTE_SMALL, ROUTE_LARGE = 0, 1, 2
+ACT_MXFP8, ACT_BF16 = 0, 1          # a8w4 (default), a16w4
 # debug stage -> (name, numpy dtype, per-row width: None = flat)
 DUMP_STAGES = {0: ("idx", np.int32), 1: ("weights", np.float32), 2: ("phys", np.int32), 3: ("pos", np.int32),
                4: ("offsets", np.int32), 5: ("xq", np.uint8), 6: ("xs", np.uint8), 7: ("hq", np.uint8),
@@ -39,6 +40,7 @@ _SIGS = {
     "mm_bind_layer": [_p, _i32],
     "mm_set_recording": [_p, _i32],
     "mm_set_route": [_p, _i32],
+    "mm_set_activation_format": [_p, _i32],
     "mm_reserve": [_p, _i64],
     "mm_forward": [_p, _p, _p, _p, _p, _i64, _p],
     "mm_read_counts": [_p, _i32, _p],
@@ -173,6 +175,10 @@ class MegaMoE:
 
     def set_route(self, route: int) -> None:
         _check(lib().mm_set_route(self._h, route), "mm_set_route")
+
+    def set_activation_format(self, act: int) -> None:
+        """ACT_MXFP8 (a8w4) or ACT_BF16 (a16w4); drops the workspace (reserve again)."""
+        _check(lib().mm_set_activation_format(self._h, act), "mm_set_activation_format")
 
     def reserve(self, max_tokens: int) -> None:
         _check(lib().mm_reserve(self._h, max_tokens), "mm_reserve")

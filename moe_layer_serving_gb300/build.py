@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmegamoe.so")
-SOURCES = ["mm_api.cu", "mm_route.cu", "mm_gemm.cu", "mm_small.cu", "mm_noalloc.cu"]
+SOURCES = ["mm_api.cu", "mm_route.cu", "mm_gemm.cu", "mm_gemm16.cu", "mm_small.cu", "mm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -35,15 +35,16 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D row-major [rows][cols] tensor map, box [box_rows][128 elements], 128-byte swizzle.
+// 2-D row-major [rows][cols] tensor map, box [box_rows][box_cols elements]
+// (128 bytes of them), 128-byte swizzle.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t cols, uint64_t rows,
-              uint64_t row_bytes, uint32_t box_rows)
+              uint64_t row_bytes, uint32_t box_rows, uint32_t box_cols = 128)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -168,6 +169,7 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
     if (c->small_max > mm::kSmallMaxTokens) c->small_max = mm::kSmallMaxTokens;
     c->large_min = env_int("MM_LARGE_M_MIN", 1024);
     if (mm::gemm_prepare(dev) != cudaSuccess || mm::small_prepare() != cudaSuccess ||
+        mm::gemm16_prepare() != cudaSuccess ||
         cudaMalloc(&c->counts, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
         cudaMemset(c->counts, 0, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
         cudaMalloc(&c->status, 2 * sizeof(int)) != cudaSuccess ||
@@ -365,6 +367,19 @@ mm_status mm_set_route(mm_handle c, mm_route r)
     return MM_OK;
 }
 
+mm_status mm_set_activation_format(mm_handle c, mm_act act)
+{
+    if (!c || (act != MM_ACT_MXFP8 && act != MM_ACT_BF16)) return MM_ERR_INVALID_ARG;
+    if (act == c->act) return MM_OK;
+    if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    cudaDeviceSynchronize();
+    free_ws(c);
+    c->cap_tokens = 0;
+    c->maps_ws = false;
+    c->act = act;
+    return MM_OK;
+}
+
 mm_status mm_reserve(mm_handle c, int64_t max_tokens)
 {
     if (!c || max_tokens < 0 || max_tokens > (int64_t(1) << 24)) return MM_ERR_INVALID_ARG;
@@ -387,9 +402,10 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     add((c->P + 1) * 4);
     add(c->P * 4);                            // first tile of each expert
     add(tiles * 4 * 4 + 8);                   // tile table, done1, num_tiles, unit counter
-    add(rows * H);
+    const int64_t eb = c->act == MM_ACT_BF16 ? 2 : 1;     // bytes per dispatched activation element
+    add(rows * H * eb);
     add(tiles * (H / 128) * 512);
-    add(rows * I);
+    add(rows * I * eb);
     add(tiles * (I / 128) * 512);
     add(rows * H * 2);
     add(64);                                  // grid barrier
@@ -417,9 +433,9 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->done1 = carve<int32_t>(p, tiles);
     c->num_tiles = carve<int32_t>(p, 2);
     c->unit_next = c->num_tiles + 1;
-    c->xq = carve<uint8_t>(p, rows * H);
+    c->xq = carve<uint8_t>(p, rows * H * eb);
     c->xs_t = carve<uint8_t>(p, tiles * (H / 128) * 512);
-    c->hq = carve<uint8_t>(p, rows * I);
+    c->hq = carve<uint8_t>(p, rows * I * eb);
     c->hs_t = carve<uint8_t>(p, tiles * (I / 128) * 512);
     c->y = carve<__nv_bfloat16>(p, rows * H);
     c->grid_bar = carve<unsigned>(p, 16);
@@ -427,12 +443,21 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->ws = ws;
     c->ws_bytes = bytes;
     for (int i = 0; i < mm::kTokBoxes; ++i) {
-        if (!make_map(&c->maps.xq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox << i) ||
-            !make_map(&c->maps.hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->hq, I, rows, I, mm::kBBox << i)) {
+        bool ok;
+        if (c->act == MM_ACT_BF16)
+            ok = make_map(&c->maps16.xd[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->xq, H, rows, H * 2, mm::kBBox << i,
+                          64) &&
+                 make_map(&c->maps16.hb[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->hq, I, rows, I * 2, mm::kBBox << i,
+                          64);
+        else
+            ok = make_map(&c->maps.xq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox << i) &&
+                 make_map(&c->maps.hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->hq, I, rows, I, mm::kBBox << i);
+        if (!ok) {
             free_ws(c);
             return MM_ERR_CUDA;
         }
     }
+    c->ws_act = c->act;
     c->cap_tokens = max_tokens;
     c->rows_cap = rows;
     c->tiles_cap = tiles;
@@ -451,8 +476,26 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(logits, 4) || (bias && !aligned(bias, 4)))
         return MM_ERR_INVALID_ARG;
     if (T > c->cap_tokens) return MM_ERR_CAPACITY;
-    if (c->route == MM_ROUTE_SMALL && T > c->small_max) return MM_ERR_CAPACITY;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool prof16 = c->prof_used < static_cast<int>(c->prof_events.size()) / 2;
+    if (c->act == MM_ACT_BF16) {
+        // a16w4: the multi-launch path with bf16 dispatch and the bf16 x MXFP4 GEMM
+        if (c->route == MM_ROUTE_SMALL) return MM_ERR_UNSUPPORTED;
+        if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_dispatch16(c, hidden, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (prof16 && cudaEventRecord(c->prof_events[2 * c->prof_used], s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_gemm16(c, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (prof16 && cudaEventRecord(c->prof_events[2 * c->prof_used + 1], s) != cudaSuccess) return MM_ERR_CUDA;
+        if (mm::launch_combine(c, out, T, s) != cudaSuccess) return MM_ERR_CUDA;
+        if (prof16) ++c->prof_used;
+        c->last_route = 2;
+        c->last_launches = 7;
+        c->last_T = T;
+        c->last_stream = s;
+        return MM_OK;
+    }
+    if (c->route == MM_ROUTE_SMALL && T > c->small_max) return MM_ERR_CAPACITY;
     const bool small = c->route == MM_ROUTE_SMALL || (c->route == MM_ROUTE_AUTO && T <= c->small_max);
     const bool prof = c->prof_used < static_cast<int>(c->prof_events.size()) / 2;
     if (small) {
@@ -549,13 +592,14 @@ static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* 
     CK(cudaMemcpy(&rows, c->off + c->P, sizeof(int32_t), cudaMemcpyDeviceToHost));
     *rows_out = rows;
     const size_t pairs = static_cast<size_t>(c->last_T) * c->k;
+    const bool a16 = c->ws_act == MM_ACT_BF16;
     switch (stage) {
         case 0: case 1: case 2: case 3: *bytes = pairs * 4; break;
         case 4: *bytes = (c->P + 1) * 4; break;
-        case 5: *bytes = static_cast<size_t>(rows) * c->H; break;
-        case 6: *bytes = static_cast<size_t>(rows) * c->H / 32; break;
-        case 7: *bytes = static_cast<size_t>(rows) * c->I; break;
-        case 8: *bytes = static_cast<size_t>(rows) * c->I / 32; break;
+        case 5: *bytes = static_cast<size_t>(rows) * c->H * (a16 ? 2 : 1); break;
+        case 6: *bytes = a16 ? 0 : static_cast<size_t>(rows) * c->H / 32; break;
+        case 7: *bytes = static_cast<size_t>(rows) * c->I * (a16 ? 2 : 1); break;
+        case 8: *bytes = a16 ? 0 : static_cast<size_t>(rows) * c->I / 32; break;
         case 9: *bytes = static_cast<size_t>(rows) * c->H * 2; break;
         case 10: *bytes = 3 * sizeof(int32_t); break;
         case 11: *bytes = static_cast<size_t>(c->sms) * 8 * sizeof(uint64_t); break;

@@ -145,12 +145,13 @@ struct GemmSmem {
     uint64_t* tmem_empty;
     uint64_t* ufull;          // [kURing] unit slot written (producer)
     uint64_t* uempty;         // [kURing] unit slot read (MMA thread + every epilogue thread)
+    uint64_t* drain;          // the MMA thread's own wait for its issued work after an abort
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     volatile int* uring;      // [kURing] unit numbers
 };
 // Barrier block (256 bytes): full[8], empty[8], tmem_full, tmem_empty,
-// ufull[4], uempty[4], the TMEM base, the abort flag and the unit ring.  Its layout does not depend on the stage
+// ufull[4], uempty[4], drain, the TMEM base, the abort flag and the unit ring.  Its layout does not depend on the stage
 // count, so one kernel can run either geometry over the same buffers.
 constexpr int kMaxStages = 8;
 __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
@@ -163,10 +164,11 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
     s.tmem_empty = s.tmem_full + 1;
     s.ufull = s.tmem_empty + 1;
     s.uempty = s.ufull + kURing;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.uempty + kURing);
+    s.drain = s.uempty + kURing;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
     s.uring = s.abort_flag + 1;
-    static_assert((2 * kMaxStages + 2 + 2 * kURing) * 8 + 8 + 4 * kURing <= 256, "barrier block");
+    static_assert((2 * kMaxStages + 3 + 2 * kURing) * 8 + 8 + 4 * kURing <= 256, "barrier block");
     return s;
 }
 
@@ -182,6 +184,7 @@ __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps
         }
         mbar_init(s.tmem_full, 1);
         mbar_init(s.tmem_empty, kEpiThreads);
+        mbar_init(s.drain, 1);
         for (int i = 0; i < kURing; ++i) {
             mbar_init(&s.ufull[i], 1);
             mbar_init(&s.uempty[i], 1 + kEpiThreads);
@@ -378,10 +381,12 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, 
         acc_phase ^= 1u;
     }
     if (*s.abort_flag) {
-        // drain issued tensor-core work before the allocation is freed
-        tc_commit(s.tmem_full);
+        // drain issued tensor-core work before the allocation is freed, on a
+        // barrier of its own: completing tmem_full here could let some epilogue
+        // threads through while others have already left on the abort flag
+        tc_commit(s.drain);
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(s.tmem_full, acc_phase))
+        while (!mbar_try_wait(s.drain, 0))
             if (globaltimer() - t0 > kWaitLimitNs / 4) break;
     }
 }

@@ -118,6 +118,31 @@ struct GemmMaps {
     CUtensorMap hq[kTokBoxes]; // e4m3 [rows][I], box 16 << i rows
 };
 
+// a16w4 GEMM (bf16 tokens): token maps over the dispatched bf16 rows and over
+// h in bf16, boxes of 64 elements x (16 << i) rows.
+struct Gemm16Maps {
+    CUtensorMap xd[kTokBoxes];   // bf16 [rows][H]
+    CUtensorMap hb[kTokBoxes];   // bf16 [rows][I]
+};
+
+struct Gemm16Args {
+    const uint8_t* w1;
+    const uint8_t* w1_sf;
+    const uint8_t* w2;
+    const uint8_t* w2_sf;
+    __nv_bfloat16* hb;      // [rows][I]
+    __nv_bfloat16* y;       // [rows][H]
+    const int* tile_expert;
+    const int* tile_row0;
+    const int* tile_rows;
+    const int* num_tiles;
+    int* done1;
+    int* unit_next;
+    int* status;
+    int H, I;
+    int fault;
+};
+
 struct GemmArgs {
     const uint8_t* w1;      // weight blocks in unit order (packed e2m1, 8 KB per block)
     const uint8_t* w2;
@@ -172,6 +197,9 @@ struct mm_ctx {
     unsigned* grid_bar = nullptr;   // fused kernel's grid barrier {count, generation}
     uint64_t* stamps = nullptr;     // fused kernel's per-CTA stage timestamps [sms][8]
     mm::GemmMaps maps{};
+    mm::Gemm16Maps maps16{};
+    int act = MM_ACT_MXFP8;          // activation format (mm_set_activation_format)
+    int ws_act = MM_ACT_MXFP8;       // format the workspace was reserved for
     bool maps_weights = false, maps_ws = false;
     // per-launch timing of the dominant kernel: event pairs, pairs recorded so far
     std::vector<cudaEvent_t> prof_events;
@@ -214,6 +242,9 @@ cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s
 cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
 cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
 cudaError_t gemm_prepare(int dev);
+cudaError_t gemm16_prepare();
+cudaError_t launch_gemm16(const mm_ctx* c, cudaStream_t s);
+cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);
 cudaError_t small_prepare();
 cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logits, const float* bias, void* out,
                          int64_t T, cudaStream_t s);

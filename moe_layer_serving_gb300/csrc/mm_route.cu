@@ -173,6 +173,20 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(const __nv_bfloat16
                          xs_t);
 }
 
+// a16w4 dispatch: token t's bf16 row copied to its k dispatch rows; one thread
+// per 16-byte chunk (one load, k stores).
+__global__ void __launch_bounds__(256) dispatch16_kernel(const uint4* __restrict__ x, int64_t T, int H, int k,
+                                                         const int32_t* __restrict__ pos, uint4* __restrict__ xd)
+{
+    const int nc = H / 8;
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t t = g / nc;
+    if (t >= T) return;
+    const int c = static_cast<int>(g % nc);
+    const uint4 v = x[t * nc + c];
+    for (int j = 0; j < k; ++j) xd[static_cast<int64_t>(pos[t * k + j]) * nc + c] = v;
+}
+
 // ---------------------------------------------------------------------------
 // combine: out[t] = bf16( sum_j w[t,j] * y[pos[t,j]] ), fp32, j in order; one
 // thread per 8 outputs (128-bit loads and stores), no atomics.
@@ -261,6 +275,14 @@ cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T
     quant_dispatch_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hidden), T, c->H,
                                                                  c->k, c->pos, c->phys, c->off, c->toff, c->xq,
                                                                  c->xs_t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s)
+{
+    const int64_t threads = T * (c->H / 8);
+    dispatch16_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const uint4*>(hidden), T, c->H, c->k,
+                                                             c->pos, reinterpret_cast<uint4*>(c->xq));
     return cudaGetLastError();
 }
 
