@@ -75,13 +75,16 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the oracle's timed sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
+    ap.add_argument("--act", choices=["mxfp8", "bf16"], default="mxfp8",
+                    help="activation format: mxfp8 (a8w4, the fused operator) or bf16 (the a16w4 variant)")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E = P (a smaller case of the same kernels, for profiler captures)")
     return ap.parse_args()
 
 
-def workload_config(cfg):
-    return {"workload": f"moe-layer-a8w4-T{cfg.T}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+def workload_config(cfg, act="mxfp8"):
+    name = "a8w4" if act == "mxfp8" else "a16w4"
+    return {"workload": f"moe-layer-{name}-T{cfg.T}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
             "P": cfg.P, "topk": cfg.k, "routing": "zipf" if cfg.zipf_s else "uniform",
             "eplb_redundant": cfg.P - cfg.E, "l2": "weights 6 GB > L2, no flush",
             "parallelism": "replicas"}
@@ -132,13 +135,13 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens):
+def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens, act="mxfp8"):
     """Tokens/s of the CPU oracle on the first n_tokens of the batch."""
     import oracle
     sel = np.arange(min(n_tokens, hidden.shape[0]))
     m, rc = pmap if pmap else (None, None)
     t0 = time.perf_counter()
-    oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel)
+    oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel, act=act)
     dt = time.perf_counter() - t0
     return sel.size / dt, dt, sel.size
 
@@ -178,10 +181,10 @@ def run_reference(args):
     pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
     n = min(args.cpu_sample, cfg.T)
     for _ in range(max(0, args.warmup and 1)):
-        oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, 1)
+        oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, 1, args.act)
     times = []
     for _ in range(args.steps):
-        _, dt, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n)
+        _, dt, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, args.act)
         times.append(dt)
     per_tok = statistics.median(times) / n
     value = 1.0 / per_tok
@@ -189,7 +192,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * cfg.T * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(cfg),
+        "data": "synthetic", "config": workload_config(cfg, args.act),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": f"first {n} of {cfg.T} tokens per step, all stages"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -229,6 +232,9 @@ def main():
     torch.cuda.empty_cache()
     if pmap:
         op.set_eplb_map(*pmap)
+    a16 = args.act == "bf16"
+    if a16:
+        op.set_activation_format(mm.ACT_BF16)
     op.reserve(cfg.T)
     op.set_recording(cfg.recording)
     x = torch.from_numpy(hidden.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -301,37 +307,38 @@ def main():
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         peaks = json.load(open(pk))
+    kname = "gemm16_kernel" if a16 else ("small_kernel" if route == 1 else "gemm_kernel")
+    wname = workload_config(cfg, args.act)["workload"]
     if cfg.T <= 512:
         alg = touched * expert_bytes(cfg)           # weight streaming: the touched experts' bytes
         achieved = alg / (kern_ms / 1e3) / 1e9
         peak = peaks.get("hbm_gbs", 6800.0)
-        kname = "small_kernel" if route == 1 else "gemm_kernel"
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": measured_traffic(kname, workload_config(cfg)["workload"]), "kernel": kname,
-                "algorithmic_bytes": alg,
+                "traffic": measured_traffic(kname, wname), "kernel": kname, "algorithmic_bytes": alg,
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
     else:
         flops = 6.0 * cfg.T * cfg.k * cfg.H * cfg.I
         achieved = flops / (kern_ms / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops", 1900.0) * 2.0   # fp8-class MMA: 2x the bf16 rate
-        kname = "small_kernel" if route == 1 else "gemm_kernel"
+        # bf16 MMAs (a16w4) against the measured bf16 rate; fp8-class MMAs at 2x it
+        mult = 1.0 if a16 else 2.0
+        peak = peaks.get("bf16_tflops", 1900.0) * mult
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": measured_traffic(kname, workload_config(cfg)["workload"]), "kernel": kname,
-                "algorithmic_flops": flops,
-                "peak_source": "measured bf16 x 2" if "bf16_tflops" in peaks else "fallback x 2"}
+                "traffic": measured_traffic(kname, wname), "kernel": kname, "algorithmic_flops": flops,
+                "peak_source": ("measured bf16" if a16 else "measured bf16 x 2") if "bf16_tflops" in peaks
+                else ("fallback" if a16 else "fallback x 2")}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3xe2m1->f32", "data": "synthetic (seeded, random-init weights)",
-        "config": workload_config(cfg), "clocks": clk, "gpu_launches": launches * args.steps,
+        "vs_baseline": None, "dtype": "bf16xe2m1->f32" if a16 else "e4m3xe2m1->f32",
+        "data": "synthetic (seeded, random-init weights)", "config": workload_config(cfg, args.act), "clocks": clk, "gpu_launches": launches * args.steps,
         "route": "small" if route == 1 else "large", "kernel_ms": kern_ms, "touched_experts": touched,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": roof,
     }
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
-        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_sample)
+        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_sample, args.act)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
                                 "sample": f"first {n} of {cfg.T} tokens, all stages, {dt:.1f} s"}
     if rank == 0:

@@ -25,14 +25,21 @@
 //       stored as GEMM2's token operand.
 //   GEMM2 unit (tile, mb): output features mb*128 .. +128.
 //
-// Warp roles (448 threads): 0 = producer (TMA for the token rows, bulk copies
-// for the packed weight rows and their scale tiles), 1 = TMEM owner + MMA
-// issuer, 2..9 = converters (warp w: TMEM lane quarter w % 4, K half
-// (w - 2) / 4 of each 128-wide stage), 10..13 = epilogue (lane quarter w % 4).
-// Four shared-memory stages pair one to one with four A slots in tensor
-// memory; the accumulator is double-buffered.  Units are handed out at run
-// time through a global counter and a ring in shared memory, GEMM1 units
-// first; a GEMM2 unit waits (bounded) for the GEMM1 units of its tile.
+// Warp roles (736 threads with 16 converter warps): 0 = weight producer (bulk copies of the packed
+// weight rows and their scale tiles; it also draws the units), 1 = TMEM owner
+// + MMA issuer, 2 = token producer (TMA for the token rows; a GEMM2 unit first
+// waits, bounded, until the GEMM1 units of its tile have published h),
+// 3..18 = converters (warp w: TMEM lane quarter w % 4, K quarter (w - 3) / 4
+// of each 128-wide stage, i.e. one 32-element scale block), 19..22 = epilogue
+// (lane quarter w % 4).  A converter warp's time per stage is a latency
+// chain (shared-memory load, conversion, tensor-memory store), so there are
+// four per scheduler, and a warp waits for its store of stage s only after it
+// has converted stage s + 1.
+// Three rings: packed weights (deep: the weight stream is what decode waits
+// on, and a converter frees a slot as soon as it has read it), token rows
+// (shallow: 32 KB a slot), and A slots in tensor memory between converters
+// and MMA.  The accumulator is double-buffered.  Units are handed out at run
+// time through a global counter and a ring in shared memory, GEMM1 units first.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -44,27 +51,44 @@
 namespace mm {
 namespace {
 
-constexpr int kT16Threads = 448;
-constexpr int kConvWarp0 = 2, kConvThreads = 256;
-constexpr int kEpi16Warp0 = 10, kEpi16Threads = 128;
-constexpr int kS16 = 4;                                    // pipeline stages (= A slots)
+#ifndef MM_CONV_WARPS
+#define MM_CONV_WARPS 16
+#endif
+constexpr int kConvWarps = MM_CONV_WARPS;                  // 8 or 16
+static_assert(kConvWarps == 8 || kConvWarps == 16, "converter warps");
+constexpr int kKParts = kConvWarps / 4;                    // K parts of a stage per lane quarter
+constexpr int kEPT = 128 / kKParts;                        // elements a converter thread converts per stage
+constexpr int kTokWarp = 2;
+constexpr int kConvWarp0 = 3, kConvThreads = 32 * kConvWarps;
+constexpr int kEpi16Warp0 = kConvWarp0 + kConvWarps, kEpi16Threads = 128;
+constexpr int kT16Threads = 32 * kEpi16Warp0 + kEpi16Threads;
+constexpr int kWRing = 12;                                 // packed-weight stages
+constexpr int kTRing = 3;                                  // token stages
+constexpr int kARing = 4;                                  // A slots in tensor memory
 constexpr int kTokHalfBytes = 128 * 128;                   // 128 rows x 64 bf16: one swizzle column
+constexpr int kTokStageBytes = 2 * kTokHalfBytes;          // K = 128 of up to 128 token rows
 constexpr int kRawBytes = 8192;                            // packed e2m1 of a stage: 128 rows x 128 K
 constexpr int kSf16Bytes = 1024;                           // one or two 512-byte scale tiles
-constexpr int kStage16Bytes = 2 * kTokHalfBytes + kRawBytes + kSf16Bytes;
-static_assert(kStage16Bytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+constexpr int kWStageBytes = kRawBytes + kSf16Bytes;
 constexpr int kURing16 = 4;
-constexpr int kSmem16Bytes = kS16 * kStage16Bytes + 256 + 1024;
+constexpr int kBar16Bytes = 512;
+constexpr int kSmem16Bytes = kTRing * kTokStageBytes + kWRing * kWStageBytes + kBar16Bytes + 1024;
+static_assert(kTokStageBytes % 1024 == 0 && kWStageBytes % 1024 == 0, "1024-byte aligned stages");
+static_assert(kSmem16Bytes <= 232448, "shared memory per block");
 // tensor memory: accumulators [0, 256) = 2 x 128 columns, A slots [256, 512) = 4 x 64
 constexpr uint32_t kTmem16Cols = 512, kAcc16Cols = 128, kASlot0 = 256, kASlotCols = 64;
 
 struct Smem16 {
-    uint8_t* stages;
-    uint64_t* full;     // [kS16] TMA bytes landed
-    uint64_t* empty;    // [kS16] the stage's MMAs finished (smem stage and A slot free)
-    uint64_t* afull;    // [kS16] A slot written by the 8 converter warps
-    uint64_t* tfull;    // [2] accumulator complete
-    uint64_t* tempty;   // [2] accumulator drained by the epilogue
+    uint8_t* tok;       // [kTRing][kTokStageBytes]
+    uint8_t* wst;       // [kWRing][kWStageBytes]
+    uint64_t* wfull;    // [kWRing] weight bytes landed
+    uint64_t* wempty;   // [kWRing] read by the 8 converter warps
+    uint64_t* tfull_;   // [kTRing] token rows landed
+    uint64_t* tempty_;  // [kTRing] the stage's MMAs finished
+    uint64_t* afull;    // [kARing] A slot written by the 8 converter warps
+    uint64_t* aempty;   // [kARing] the slot's MMAs finished
+    uint64_t* dfull;    // [2] accumulator complete
+    uint64_t* dempty;   // [2] accumulator drained by the epilogue
     uint64_t* ufull;    // [kURing16] unit slot written
     uint64_t* uempty;   // [kURing16] unit slot read by every consumer
     uint64_t* drain;    // the MMA thread's own wait for its issued work after an abort
@@ -76,22 +100,41 @@ struct Smem16 {
 __device__ __forceinline__ Smem16 smem16(uint8_t* base)
 {
     Smem16 s;
-    s.stages = base;
-    uint64_t* b = reinterpret_cast<uint64_t*>(base + kS16 * kStage16Bytes);
-    s.full = b;
-    s.empty = s.full + kS16;
-    s.afull = s.empty + kS16;
-    s.tfull = s.afull + kS16;
-    s.tempty = s.tfull + 2;
-    s.ufull = s.tempty + 2;
+    s.tok = base;
+    s.wst = base + kTRing * kTokStageBytes;
+    uint64_t* b = reinterpret_cast<uint64_t*>(s.wst + kWRing * kWStageBytes);
+    s.wfull = b;
+    s.wempty = s.wfull + kWRing;
+    s.tfull_ = s.wempty + kWRing;
+    s.tempty_ = s.tfull_ + kTRing;
+    s.afull = s.tempty_ + kTRing;
+    s.aempty = s.afull + kARing;
+    s.dfull = s.aempty + kARing;
+    s.dempty = s.dfull + 2;
+    s.ufull = s.dempty + 2;
     s.uempty = s.ufull + kURing16;
     s.drain = s.uempty + kURing16;
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
     s.uring = s.abort_flag + 1;
-    static_assert((3 * kS16 + 5 + 2 * kURing16) * 8 + 8 + 4 * kURing16 <= 256, "barrier block");
+    static_assert((2 * kWRing + 2 * kTRing + 2 * kARing + 4 + 2 * kURing16 + 1) * 8 + 8 + 4 * kURing16 <= kBar16Bytes,
+                  "barrier block");
     return s;
 }
+
+// A ring position: slot and phase, advanced once per stage.
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance()
+    {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 struct Unit16 {
     int phase;       // 1 or 2
@@ -143,17 +186,7 @@ __device__ __forceinline__ bool decode16(const Gemm16Args& g, int u, Unit16& un)
     return true;
 }
 
-struct UQ {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void advance()
-    {
-        if (++slot == kURing16) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
-};
+using UQ = Ring<kURing16>;
 
 __device__ __forceinline__ bool push16(const Gemm16Args& g, const Smem16& s, UQ& q, int& u)
 {
@@ -175,20 +208,21 @@ __device__ __forceinline__ bool pop16(const Gemm16Args& g, const Smem16& s, UQ& 
 }
 
 // ---- FP4 -> bf16 ---------------------------------------------------------------
-// An e2m1 nibble s|e1 e0|m placed at bf16 bits 15 | 8..7 | 6 reads, as a bf16
-// bit pattern, (e2m1 value) x 2^-126: the nibble's exponent field lands in the
-// low bits of the bf16 exponent (bias 1 vs 127) and its subnormal 0.5 becomes
-// the bf16 subnormal 2^-127.  One multiply by 2^(X + 126) then gives the
-// element times its block scale 2^X, exactly (two significant bits at most);
-// for X + 126 > 127 the factor is split in two.
-// t: one packed byte (element 2i in the low nibble) -> bf16x2 (element 2i low).
-__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t t, __nv_bfloat162 f1)
+// Bit placement: a nibble n = s|e1 e0|m spread so that e1 e0 m sit at bf16
+// bits 8..6 and s at bit 15 reads, as a bf16 bit pattern, (e2m1 value) x
+// 2^-126 (its exponent field lands in the low bits of the bf16 exponent, bias
+// 1 against 127, and its subnormal 0.5 becomes the bf16 subnormal 2^-127).
+// For an element pair, x0 (even element) in bits 0..3 and x1 in bits 16..19 of
+// v, one multiply by 4160 = 2^12 + 2^6 adds v << 6 (magnitudes to 6..8 and
+// 22..24) and v << 12 (signs to 15 and 31) without overlapping carries, and a
+// mask keeps those eight bits.  One bf16 multiply by 2^(X + 126) then gives
+// the element times its block scale 2^X exactly (two significant bits at
+// most); for X + 126 > 127 the factor is split in two.
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel)
 {
-    const uint32_t y = t * 0x1001u;            // low nibble at bits 0..3, high nibble at 16..19
-    const uint32_t r = ((y & 0x00070007u) << 6) | ((y & 0x00080008u) << 12);
-    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&r);
-    v = __hmul2(v, f1);
-    return *reinterpret_cast<const uint32_t*>(&v);
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
 }
 
 __device__ __forceinline__ __nv_bfloat162 bf16x2_pow2(int e)     // 2^e, -133 < e <= 127: normal range used
@@ -198,36 +232,56 @@ __device__ __forceinline__ __nv_bfloat162 bf16x2_pow2(int e)     // 2^e, -133 < 
     return *reinterpret_cast<const __nv_bfloat162*>(&r);
 }
 
-// 32 packed bytes (64 elements, two 32-element blocks with scale bytes s0, s1)
-// -> 32 bf16x2 words.
-__device__ __forceinline__ void convert64(const uint4 q0, const uint4 q1, uint32_t s0, uint32_t s1,
-                                          uint32_t (&w)[32])
+// 4 packed bytes (8 elements, element 2i in the low nibble of byte i) ->
+// 4 bf16x2 words (element 2i in the low half), times f1.
+__device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t w, __nv_bfloat162 f1, uint32_t* o)
 {
-    const uint32_t in[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t ev = w & 0x0F0F0F0Fu;            // even elements' nibbles
+    const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;     // odd elements' nibbles
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-        const int sb = static_cast<int>(blk == 0 ? s0 : s1);     // scale byte: X = sb - 127
-        const bool wide = sb >= 129;                               // X + 126 > 127
-        const __nv_bfloat162 f1 = bf16x2_pow2(wide ? 127 : sb - 1);
+    for (int j = 0; j < 4; ++j) {
+        // byte 0 = even nibble j, byte 2 = odd nibble j; bytes 1 and 3 replicate
+        // the sign bit of byte 0 of ev, which is 0 (a nibble is below 0x80)
+        const uint32_t v = prmt_b32(ev, od, static_cast<uint32_t>(j) | 0x80u | ((4u + j) << 8) | 0x8000u);
+        const uint32_t r = (v * 4160u) & 0x81C081C0u;
+        __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&r);
+        x = __hmul2(x, f1);
+        o[j] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+}
+
+// 16 packed bytes (32 elements, one block with scale byte sb) -> 16 bf16x2 words.
+__device__ __forceinline__ void convert32(const uint4 q, uint32_t sb_u, uint32_t* w)
+{
+    const int sb = static_cast<int>(sb_u);     // X = sb - 127
+    const bool wide = sb >= 129;               // X + 126 > 127
+    const __nv_bfloat162 f1 = bf16x2_pow2(wide ? 127 : sb - 1);
+    e2m1x8_to_bf16x8(q.x, f1, w);
+    e2m1x8_to_bf16x8(q.y, f1, w + 4);
+    e2m1x8_to_bf16x8(q.z, f1, w + 8);
+    e2m1x8_to_bf16x8(q.w, f1, w + 12);
+    if (wide) {
+        const __nv_bfloat162 f2 = bf16x2_pow2(sb - 128);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t word = in[4 * blk + i];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) w[16 * blk + 4 * i + b] = e2m1x2_to_bf16x2((word >> (8 * b)) & 0xFFu, f1);
-        }
-        if (wide) {
-            const __nv_bfloat162 f2 = bf16x2_pow2(sb - 128);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[16 * blk + i]);
-                v = __hmul2(v, f2);
-                w[16 * blk + i] = *reinterpret_cast<const uint32_t*>(&v);
-            }
+        for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+            v = __hmul2(v, f2);
+            w[i] = *reinterpret_cast<const uint32_t*>(&v);
         }
     }
 }
 
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* r)
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -269,20 +323,60 @@ __device__ __forceinline__ int ld_acquire_i32(const int* p)
     return v;
 }
 
-// ---- producer -----------------------------------------------------------------
-__device__ __forceinline__ void producer16(const Gemm16Maps& maps, const Gemm16Args& g, const Smem16& s)
+// ---- weight producer (warp 0, one thread): draws the units --------------------
+__device__ __forceinline__ void wproducer16(const Gemm16Args& g, const Smem16& s)
 {
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_a = policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    int armed[kS16];
-    for (int i = 0; i < kS16; ++i) armed[i] = -1;
+    Ring<kWRing> w;
+    int armed[kWRing];
+    for (int i = 0; i < kWRing; ++i) armed[i] = -1;
     Unit16 un;
     UQ q;
     for (;;) {
         int u;
         if (!push16(g, s, q, u) || *s.abort_flag || !decode16(g, u, un)) break;
+        const uint32_t bytes = kRawBytes + (un.phase == 1 ? 1024u : 512u);
+        for (int ks = 0; ks < un.ksteps; ++ks) {
+            if (!mbar_wait(&s.wempty[w.slot], w.phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
+            uint8_t* raw = s.wst + w.slot * kWStageBytes;
+            uint8_t* sf = raw + kRawBytes;
+            mbar_arrive_expect_tx(&s.wfull[w.slot], bytes);
+            armed[w.slot] = static_cast<int>(w.phase);
+            const int64_t blk = un.wblk + 2 * ks;
+            if (un.phase == 1) {
+                // the unit's 64-row halves of the gate block and of the up block
+                bulk_load(raw, g.w1 + blk * 8192 + un.sel * 4096, 4096, &s.wfull[w.slot]);
+                bulk_load(raw + 4096, g.w1 + (blk + 1) * 8192 + un.sel * 4096, 4096, &s.wfull[w.slot]);
+                bulk_load(sf, g.w1_sf + blk * 512, 1024, &s.wfull[w.slot]);
+            } else {
+                bulk_load(raw, g.w2 + blk * 8192, 8192, &s.wfull[w.slot]);
+                bulk_load(sf, g.w2_sf + blk * 512, 512, &s.wfull[w.slot]);
+            }
+            w.advance();
+        }
+    }
+    if (*s.abort_flag) {
+        // let copies already in flight land before the CTA exits
+        for (int i = 0; i < kWRing; ++i) {
+            if (armed[i] < 0) continue;
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&s.wfull[i], static_cast<uint32_t>(armed[i])))
+                if (globaltimer() - t0 > kWaitLimitNs / 4) break;
+        }
+    }
+}
+
+// ---- token producer (warp 2, one thread) ------------------------------------------
+__device__ __forceinline__ void tproducer16(const Gemm16Maps& maps, const Gemm16Args& g, const Smem16& s)
+{
+    const uint64_t pol_a = policy_evict_last();
+    Ring<kTRing> t;
+    int armed[kTRing];
+    for (int i = 0; i < kTRing; ++i) armed[i] = -1;
+    Unit16 un;
+    UQ q;
+    for (;;) {
+        int u;
+        if (!pop16(g, s, q, u) || *s.abort_flag || !decode16(g, u, un)) break;
         const CUtensorMap* tmap = un.phase == 1 ? &maps.xd[un.tbox] : &maps.hb[un.tbox];
         if (un.phase == 2) {
             const int need = g.I / 64 + (g.fault == kFaultGemmDependency ? 1 : 0);
@@ -300,115 +394,156 @@ __device__ __forceinline__ void producer16(const Gemm16Maps& maps, const Gemm16A
             fence_proxy_async_global();
             if (*s.abort_flag) break;
         }
-        const uint32_t tok_bytes = 2u * (16u << un.tbox) * 128u;
-        const uint32_t sf_bytes = un.phase == 1 ? 1024u : 512u;
-        const uint32_t bytes = tok_bytes + kRawBytes + sf_bytes;
+        const uint32_t bytes = 2u * (16u << un.tbox) * 128u;
         for (int ks = 0; ks < un.ksteps; ++ks) {
-            if (!mbar_wait(&s.empty[stage], phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
-            uint8_t* st = s.stages + stage * kStage16Bytes;
-            uint8_t* raw = st + 2 * kTokHalfBytes;
-            uint8_t* sf = raw + kRawBytes;
-            mbar_arrive_expect_tx(&s.full[stage], bytes);
-            armed[stage] = static_cast<int>(phase);
-            tma_load_2d(st, tmap, ks * 128, un.row0, &s.full[stage], pol_a);
-            tma_load_2d(st + kTokHalfBytes, tmap, ks * 128 + 64, un.row0, &s.full[stage], pol_a);
-            const int64_t blk = un.wblk + 2 * ks;
-            if (un.phase == 1) {
-                // the unit's 64-row halves of the gate block and of the up block
-                bulk_load(raw, g.w1 + blk * 8192 + un.sel * 4096, 4096, &s.full[stage]);
-                bulk_load(raw + 4096, g.w1 + (blk + 1) * 8192 + un.sel * 4096, 4096, &s.full[stage]);
-                bulk_load(sf, g.w1_sf + blk * 512, 1024, &s.full[stage]);
-            } else {
-                bulk_load(raw, g.w2 + blk * 8192, 8192, &s.full[stage]);
-                bulk_load(sf, g.w2_sf + blk * 512, 512, &s.full[stage]);
-            }
-            if (++stage == kS16) {
-                stage = 0;
-                phase ^= 1u;
-            }
+            if (!mbar_wait(&s.tempty_[t.slot], t.phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
+            uint8_t* st = s.tok + t.slot * kTokStageBytes;
+            mbar_arrive_expect_tx(&s.tfull_[t.slot], bytes);
+            armed[t.slot] = static_cast<int>(t.phase);
+            tma_load_2d(st, tmap, ks * 128, un.row0, &s.tfull_[t.slot], pol_a);
+            tma_load_2d(st + kTokHalfBytes, tmap, ks * 128 + 64, un.row0, &s.tfull_[t.slot], pol_a);
+            t.advance();
         }
     }
     if (*s.abort_flag) {
-        for (int i = 0; i < kS16; ++i) {
+        for (int i = 0; i < kTRing; ++i) {
             if (armed[i] < 0) continue;
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(&s.full[i], static_cast<uint32_t>(armed[i])))
+            while (!mbar_try_wait(&s.tfull_[i], static_cast<uint32_t>(armed[i])))
                 if (globaltimer() - t0 > kWaitLimitNs / 4) break;
         }
     }
 }
 
-// ---- MMA issuer ---------------------------------------------------------------
+// ---- MMA issuer (warp 1, all lanes) ------------------------------------------
+// The whole warp runs the loop, so every operand of an MMA is computed
+// warp-uniformly; one elected lane issues the tensor-core instructions.  (An
+// MMA of small N is issued in a few tens of cycles; the issuing thread's own
+// operand arithmetic is what would otherwise set the rate.)
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
+__device__ __forceinline__ bool pop16_warp(const Gemm16Args& g, const Smem16& s, UQ& q, int& u)
+{
+    const bool ok = mbar_wait(&s.ufull[q.slot], q.phase, g.status, s.abort_flag, kSiteUnitQueue);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    u = s.uring[q.slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.uempty[q.slot]);
+    q.advance();
+    return true;
+}
+
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Gemm16Args& g, const Smem16& s,
+                                          int site)
+{
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, g.status, s.abort_flag, site));
+}
+
 __device__ __forceinline__ void mma16(const Gemm16Args& g, const Smem16& s, uint32_t tmem)
 {
-    static_assert(kS16 * kStage16Bytes + 1024 < (1 << 18), "descriptor address field");
-    const uint64_t b_desc0 = desc_kmajor_sw128(s.stages);
-    constexpr uint64_t kStageDesc = kStage16Bytes >> 4, kHalfDesc = kTokHalfBytes >> 4;
-    int stage = 0;
-    uint32_t phase = 0;
+    static_assert(kTRing * kTokStageBytes + 1024 < (1 << 18), "descriptor address field");
+    const uint64_t b_desc0 = desc_kmajor_sw128(s.tok);
+    constexpr uint64_t kStageDesc = kTokStageBytes >> 4, kHalfDesc = kTokHalfBytes >> 4;
+    Ring<kTRing> t;
+    Ring<kARing> a;
     int acc = 0;       // accumulators used so far: buffer acc & 1, phase (acc >> 1) & 1
+    bool aborted = false;
     Unit16 un;
     UQ q;
     for (;;) {
         int u;
-        if (!pop16(g, s, q, u) || *s.abort_flag || !decode16(g, u, un)) break;
+        if (!pop16_warp(g, s, q, u) || *s.abort_flag || !decode16(g, u, un)) break;
         const int buf = acc & 1;
         const uint32_t aph = static_cast<uint32_t>(acc >> 1) & 1u;
-        if (!mbar_wait(&s.tempty[buf], aph ^ 1u, g.status, s.abort_flag, kSiteMmaTmemEmpty)) break;
+        if (!wait_warp(&s.dempty[buf], aph ^ 1u, g, s, kSiteMmaTmemEmpty)) {
+            aborted = true;
+            break;
+        }
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf) * kAcc16Cols;
         const uint32_t id = idesc_bf16(static_cast<uint32_t>(un.n));
         for (int ks = 0; ks < un.ksteps; ++ks) {
-            // the token rows (TMA) and the A slot (converters) of this stage
-            if (!mbar_wait(&s.full[stage], phase, g.status, s.abort_flag, kSiteMmaFull)) break;
-            if (!mbar_wait(&s.afull[stage], phase, g.status, s.abort_flag, kSiteMmaFull)) break;
-            tc_fence_after();
-            const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * kStageDesc;
-            const uint32_t a = tmem + kASlot0 + static_cast<uint32_t>(stage) * kASlotCols;
-            // K = 128: eight MMAs of K = 16; the token rows' K halves are two swizzle columns
-            if (ks == 0)
-                mma_bf16_tmem_a<false>(d, a, bd, id);
-            else
-                mma_bf16_tmem_a<true>(d, a, bd, id);
-            mma_bf16_tmem_a<true>(d, a + 8, bd + 2, id);
-            mma_bf16_tmem_a<true>(d, a + 16, bd + 4, id);
-            mma_bf16_tmem_a<true>(d, a + 24, bd + 6, id);
-            mma_bf16_tmem_a<true>(d, a + 32, bd + kHalfDesc, id);
-            mma_bf16_tmem_a<true>(d, a + 40, bd + kHalfDesc + 2, id);
-            mma_bf16_tmem_a<true>(d, a + 48, bd + kHalfDesc + 4, id);
-            mma_bf16_tmem_a<true>(d, a + 56, bd + kHalfDesc + 6, id);
-            tc_commit(&s.empty[stage]);
-            if (++stage == kS16) {
-                stage = 0;
-                phase ^= 1u;
+            // this stage's token rows (TMA) and A slot (converters)
+            if (!wait_warp(&s.tfull_[t.slot], t.phase, g, s, kSiteMmaFull) ||
+                !wait_warp(&s.afull[a.slot], a.phase, g, s, kSiteMmaFull)) {
+                aborted = true;
+                break;
             }
+            tc_fence_after();
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(t.slot) * kStageDesc;
+            const uint32_t at = tmem + kASlot0 + static_cast<uint32_t>(a.slot) * kASlotCols;
+            if (elect_one()) {
+                // K = 128: eight MMAs of K = 16; the token rows' K halves are two swizzle columns
+                if (ks == 0)
+                    mma_bf16_tmem_a<false>(d, at, bd, id);
+                else
+                    mma_bf16_tmem_a<true>(d, at, bd, id);
+                mma_bf16_tmem_a<true>(d, at + 8, bd + 2, id);
+                mma_bf16_tmem_a<true>(d, at + 16, bd + 4, id);
+                mma_bf16_tmem_a<true>(d, at + 24, bd + 6, id);
+                mma_bf16_tmem_a<true>(d, at + 32, bd + kHalfDesc, id);
+                mma_bf16_tmem_a<true>(d, at + 40, bd + kHalfDesc + 2, id);
+                mma_bf16_tmem_a<true>(d, at + 48, bd + kHalfDesc + 4, id);
+                mma_bf16_tmem_a<true>(d, at + 56, bd + kHalfDesc + 6, id);
+                tc_commit(&s.tempty_[t.slot]);
+                tc_commit(&s.aempty[a.slot]);
+            }
+            __syncwarp();
+            t.advance();
+            a.advance();
         }
-        if (*s.abort_flag) break;
-        tc_commit(&s.tfull[buf]);
+        if (aborted || *s.abort_flag) break;
+        if (elect_one()) tc_commit(&s.dfull[buf]);
+        __syncwarp();
         ++acc;
     }
     if (*s.abort_flag) {
         // drain issued tensor-core work before the allocation is freed, on a
         // barrier no other role waits on
-        tc_commit(s.drain);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(s.drain, 0))
-            if (globaltimer() - t0 > kWaitLimitNs / 4) break;
+        if (elect_one()) {
+            tc_commit(s.drain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(s.drain, 0))
+                if (globaltimer() - t0 > kWaitLimitNs / 4) break;
+        }
+        __syncwarp();
     }
 }
 
-// ---- converters: warps 2..9 -----------------------------------------------------
+// ---- converters: warps 3..18 -----------------------------------------------------
 // Thread (quarter qd, lane l) writes A row r = 32 qd + l; its warp covers the
-// K half kh (64 elements) of every stage.
+// K quarter kq (32 elements, one scale block) of every stage.  A weight slot
+// is released once the warp has converted what it read; the tensor-memory
+// store of stage s is waited for (and its A slot published) after stage s + 1
+// is converted, and at the end of every unit.
 __device__ __forceinline__ void convert16(const Gemm16Args& g, const Smem16& s, uint32_t tmem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qd = warp & 3, kh = (warp - kConvWarp0) >> 2;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kASlot0 + 32u * kh;
-    int stage = 0;
-    uint32_t phase = 0;
+    const int qd = warp & 3, kq = (warp - kConvWarp0) >> 2;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kASlot0 + (kEPT / 2u) * kq;
+    Ring<kWRing> w;
+    Ring<kARing> a;
+    int pending = -1;          // A slot whose store is in flight
     Unit16 un;
     UQ q;
+    auto publish = [&]() {
+        if (pending >= 0) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.afull[pending]);
+            pending = -1;
+        }
+    };
     for (;;) {
         int u;
         if (!pop16(g, s, q, u) || *s.abort_flag || !decode16(g, u, un)) break;
@@ -426,31 +561,46 @@ __device__ __forceinline__ void convert16(const Gemm16Args& g, const Smem16& s, 
             sfrow = r;
             sftile = 0;
         }
-        const int sfo = sftile + (sfrow % 32) * 16 + (sfrow / 32) * 4 + 2 * kh;
+        src += (kEPT / 2) * kq;
+        const int sfo = kRawBytes + sftile + (sfrow % 32) * 16 + (sfrow / 32) * 4 + (kEPT / 32) * kq;
+        bool ok = true;
         for (int ks = 0; ks < un.ksteps; ++ks) {
-            // warp-uniform: after an abort the producer still lets copies in
-            // flight land, so lanes could otherwise disagree before the
-            // warp-collective tensor-memory store
-            const bool ok = mbar_wait(&s.full[stage], phase, g.status, s.abort_flag, kSiteMmaFull);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            const uint8_t* raw = s.stages + stage * kStage16Bytes + 2 * kTokHalfBytes;
-            const uint4* pk = reinterpret_cast<const uint4*>(raw + src + 32 * kh);
-            const uint4 q0 = pk[0], q1 = pk[1];
-            const uint8_t* sf = raw + kRawBytes + sfo;
-            uint32_t w[32];
-            convert64(q0, q1, sf[0], sf[1], w);
-            tmem_st_32x32b_x32(lane_addr + static_cast<uint32_t>(stage) * kASlotCols, w);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.afull[stage]);
-            if (++stage == kS16) {
-                stage = 0;
-                phase ^= 1u;
+            // warp-uniform decisions: after an abort the producers still let
+            // copies in flight land, so lanes could otherwise disagree before
+            // the warp-collective tensor-memory store
+            ok = mbar_wait(&s.wfull[w.slot], w.phase, g.status, s.abort_flag, kSiteMmaFull);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+                ok = false;
+                break;
             }
+            const uint8_t* raw = s.wst + w.slot * kWStageBytes;
+            uint32_t cw[kEPT / 2];
+#pragma unroll
+            for (int b = 0; b < kEPT / 32; ++b) {
+                const uint4 pk = reinterpret_cast<const uint4*>(raw + src)[b];
+                convert32(pk, raw[sfo + b], cw + 16 * b);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.wempty[w.slot]);
+            w.advance();
+            publish();
+            ok = mbar_wait(&s.aempty[a.slot], a.phase ^ 1u, g.status, s.abort_flag, kSiteMmaTmemEmpty);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if constexpr (kEPT == 32)
+                tmem_st_32x32b_x16(lane_addr + static_cast<uint32_t>(a.slot) * kASlotCols, cw);
+            else
+                tmem_st_32x32b_x32(lane_addr + static_cast<uint32_t>(a.slot) * kASlotCols, cw);
+            pending = a.slot;
+            a.advance();
         }
-        if (*s.abort_flag) break;
+        if (ok) publish();
+        if (!ok || *s.abort_flag) break;
     }
+    if (pending >= 0) tmem_st_wait();    // no store may be left in flight when the CTA tears down
 }
 
 // 16 consecutive accumulator columns of this warp's 32 rows
@@ -476,7 +626,7 @@ __device__ __forceinline__ void epilogue16(const Gemm16Args& g, const Smem16& s,
         int u;
         if (!pop16(g, s, q, u) || *s.abort_flag || !decode16(g, u, un)) break;
         const int buf = acc & 1;
-        if (!mbar_wait(&s.tfull[buf], static_cast<uint32_t>(acc >> 1) & 1u, g.status, s.abort_flag,
+        if (!mbar_wait(&s.dfull[buf], static_cast<uint32_t>(acc >> 1) & 1u, g.status, s.abort_flag,
                        kSiteEpiTmemFull))
             break;
         tc_fence_after();
@@ -507,7 +657,7 @@ __device__ __forceinline__ void epilogue16(const Gemm16Args& g, const Smem16& s,
             }
         }
         tc_fence_before();
-        mbar_arrive(&s.tempty[buf]);
+        mbar_arrive(&s.dempty[buf]);
         if (un.phase == 1) {
             // publish this unit's share of hb for the tile's GEMM2 units
             fence_proxy_async_global();
@@ -527,18 +677,26 @@ __global__ void __launch_bounds__(kT16Threads, 1)
     const Smem16 s = smem16(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kS16; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
+        for (int i = 0; i < kWRing; ++i) {
+            mbar_init(&s.wfull[i], 1);
+            mbar_init(&s.wempty[i], kConvThreads / 32);
+        }
+        for (int i = 0; i < kTRing; ++i) {
+            mbar_init(&s.tfull_[i], 1);
+            mbar_init(&s.tempty_[i], 1);
+        }
+        for (int i = 0; i < kARing; ++i) {
             mbar_init(&s.afull[i], kConvThreads / 32);
+            mbar_init(&s.aempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.tfull[i], 1);
-            mbar_init(&s.tempty[i], kEpi16Threads);
+            mbar_init(&s.dfull[i], 1);
+            mbar_init(&s.dempty[i], kEpi16Threads);
         }
         for (int i = 0; i < kURing16; ++i) {
             mbar_init(&s.ufull[i], 1);
-            mbar_init(&s.uempty[i], 1 + kConvThreads + kEpi16Threads);
+            // consumers: token producer, MMA thread, converters, epilogue
+            mbar_init(&s.uempty[i], 2 + kConvThreads + kEpi16Threads);
         }
         mbar_init(s.drain, 1);
         *s.abort_flag = 0;
@@ -557,9 +715,11 @@ __global__ void __launch_bounds__(kT16Threads, 1)
     tc_fence_after();
     const uint32_t tmem = *s.tmem_slot;
     if (warp == 0) {
-        if (lane == 0) producer16(maps, g, s);
+        if (lane == 0) wproducer16(g, s);
     } else if (warp == 1) {
-        if (lane == 0) mma16(g, s, tmem);
+        mma16(g, s, tmem);
+    } else if (warp == kTokWarp) {
+        if (lane == 0) tproducer16(maps, g, s);
     } else if (warp < kEpi16Warp0) {
         convert16(g, s, tmem);
     } else {
