@@ -326,11 +326,25 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
     }
 }
 
-// ---- MMA issuer: one thread ---------------------------------------------------
-// Descriptors are built once; a stage only adds its offset (the address field
-// of a descriptor counts 16-byte units and every stage lies below 256 KB, so
-// the add never carries out of that field).  The instruction descriptors of a
-// unit are formed once per unit.
+// ---- MMA issuer: warp 1, all lanes --------------------------------------------
+// The whole warp runs the loop, so descriptors and addresses are computed
+// warp-uniformly; one elected lane issues the tensor-core instructions (the
+// issuing thread's own operand arithmetic otherwise sets the rate of small
+// MMAs).  Descriptors are built once; a stage only adds its offset (the
+// address field of a descriptor counts 16-byte units and every stage lies
+// below 256 KB, so the add never carries out of that field).  The instruction
+// descriptors of a unit are formed once per unit.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
 template <class G>
 __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, const GemmSmem& s, uint32_t tmem)
 {
@@ -342,52 +356,74 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, 
     static_assert(kStages * G::kStageBytes + 1024 < (1 << 18), "descriptor address field");
     constexpr uint64_t kStageDesc = G::kStageBytes >> 4, kSfDesc = kSFBytes >> 4;
     const uint32_t t_sfa = tmem + kColSFA, t_sfb = tmem + kColSFB;
+    const int lane = threadIdx.x & 31;
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
+    bool aborted = false;
     Unit un;
     UnitQueue q;
     for (;;) {
-        int u;
-        if (!pop_unit(g, s, q, u) || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
-        if (!mbar_wait(s.tmem_empty, acc_phase ^ 1u, g.status, s.abort_flag, kSiteMmaTmemEmpty)) break;
+        // the unit (every lane reads it; lane 0 accounts for the warp)
+        const bool got = mbar_wait(&s.ufull[q.slot], q.phase, g.status, s.abort_flag, kSiteUnitQueue);
+        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        const int u = s.uring[q.slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.uempty[q.slot]);
+        q.advance();
+        if (*s.abort_flag || !decode_unit(g, tv, u, un)) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(s.tmem_empty, acc_phase ^ 1u, g.status, s.abort_flag,
+                                               kSiteMmaTmemEmpty))) {
+            aborted = true;
+            break;
+        }
         tc_fence_after();
         const uint32_t n = static_cast<uint32_t>(un.nw * kTile);
         const uint32_t id0 = idesc_e4m3_e2m1(n, 0), id1 = idesc_e4m3_e2m1(n, 1);
         const uint32_t id2 = idesc_e4m3_e2m1(n, 2), id3 = idesc_e4m3_e2m1(n, 3);
         const bool two = un.nw == 2;
         for (int ks = 0; ks < un.ksteps; ++ks) {
-            if (!mbar_wait(&s.full[stage], phase, g.status, s.abort_flag, kSiteMmaFull)) break;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.full[stage], phase, g.status, s.abort_flag, kSiteMmaFull))) {
+                aborted = true;
+                break;
+            }
             tc_fence_after();
             const uint64_t off = static_cast<uint64_t>(stage) * kStageDesc;
             const uint64_t ad = a_desc0 + off, bd = b_desc0 + off, sd = sf_desc0 + off;
-            tc_cp_32x128b_x4(t_sfa, sd);
-            tc_cp_32x128b_x4(t_sfb, sd + kSfDesc);
-            if (two) tc_cp_32x128b_x4(t_sfb + 4, sd + 2 * kSfDesc);
-            if (ks == 0)
-                mma_mxf8f6f4_c<false>(tmem, ad, bd, id0, t_sfa, t_sfb);
-            else
-                mma_mxf8f6f4_c<true>(tmem, ad, bd, id0, t_sfa, t_sfb);
-            mma_mxf8f6f4_c<true>(tmem, ad + 2, bd + 2, id1, t_sfa, t_sfb);
-            mma_mxf8f6f4_c<true>(tmem, ad + 4, bd + 4, id2, t_sfa, t_sfb);
-            mma_mxf8f6f4_c<true>(tmem, ad + 6, bd + 6, id3, t_sfa, t_sfb);
-            tc_commit(&s.empty[stage]);
+            if (elect_one()) {
+                tc_cp_32x128b_x4(t_sfa, sd);
+                tc_cp_32x128b_x4(t_sfb, sd + kSfDesc);
+                if (two) tc_cp_32x128b_x4(t_sfb + 4, sd + 2 * kSfDesc);
+                if (ks == 0)
+                    mma_mxf8f6f4_c<false>(tmem, ad, bd, id0, t_sfa, t_sfb);
+                else
+                    mma_mxf8f6f4_c<true>(tmem, ad, bd, id0, t_sfa, t_sfb);
+                mma_mxf8f6f4_c<true>(tmem, ad + 2, bd + 2, id1, t_sfa, t_sfb);
+                mma_mxf8f6f4_c<true>(tmem, ad + 4, bd + 4, id2, t_sfa, t_sfb);
+                mma_mxf8f6f4_c<true>(tmem, ad + 6, bd + 6, id3, t_sfa, t_sfb);
+                tc_commit(&s.empty[stage]);
+            }
+            __syncwarp();
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        if (*s.abort_flag) break;
-        tc_commit(s.tmem_full);
+        if (aborted || *s.abort_flag) break;
+        if (elect_one()) tc_commit(s.tmem_full);
+        __syncwarp();
         acc_phase ^= 1u;
     }
     if (*s.abort_flag) {
         // drain issued tensor-core work before the allocation is freed, on a
         // barrier of its own: completing tmem_full here could let some epilogue
         // threads through while others have already left on the abort flag
-        tc_commit(s.drain);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(s.drain, 0))
-            if (globaltimer() - t0 > kWaitLimitNs / 4) break;
+        if (elect_one()) {
+            tc_commit(s.drain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(s.drain, 0))
+                if (globaltimer() - t0 > kWaitLimitNs / 4) break;
+        }
+        __syncwarp();
     }
 }
 
@@ -519,7 +555,7 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
     if (warp == 0) {
         if (lane == 0) producer_loop<G>(maps, g, tv, s);
     } else if (warp == 1) {
-        if (lane == 0) mma_loop<G>(g, tv, s, tmem);
+        mma_loop<G>(g, tv, s, tmem);
     } else {
         epilogue_loop(g, tv, s, tmem);
     }
