@@ -141,17 +141,27 @@ def _check_routing(cfg, res, logits, bias, map_rc):
     return idx, w, phys
 
 
-def assert_out_close_a16(got_bits, ref_bits, what=""):
-    """a16w4 layer tolerance: relative L2 <= 4e-3 and every |err| within one
-    bf16 step of the element (2^-7 |ref|) plus 0.01 rms(ref).  The GPU path
-    rounds y to bf16 before the combine (the oracle keeps fp32), so an output
-    may land on the neighbouring bf16 value; nothing else should move it."""
+def pair_magnitude(ref, k):
+    """sum_j |w[t,j] * y[t,j]| per output element, from an oracle result."""
+    w = np.abs(ref["w"].astype(np.float64))
+    y = np.abs(ref["y"].astype(np.float64)).reshape(w.shape[0], k, -1)
+    return (w[:, :, None] * y).sum(1)
+
+
+def assert_out_close_a16(got_bits, ref_bits, what="", mag=None):
+    """a16w4 layer tolerance: relative L2 <= 4e-3, and every |err| within one
+    bf16 step of the element and of the summed terms, 2^-7 (|ref| + sum_j
+    |w_j y_j|), plus 0.01 rms(ref).  The GPU path rounds y to bf16 before the
+    combine (the oracle keeps fp32), which moves a sum by up to 2^-9 of its
+    terms' magnitude -- large next to a sum whose terms cancel -- and the
+    output may land on the neighbouring bf16 value; the rms term covers the
+    rare h that rounds to the other bf16 neighbour."""
     got, ref = bf16_f64(got_bits), bf16_f64(ref_bits)
     err = got - ref
     rms = np.sqrt(np.mean(ref ** 2))
     rel = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300)
     assert rel <= 4e-3, f"{what} relative L2 {rel:.3e}"
-    bound = 2.0 ** -7 * np.abs(ref) + 0.01 * rms
+    bound = 2.0 ** -7 * (np.abs(ref) + (0.0 if mag is None else mag)) + 0.01 * rms
     worst = np.argmax(np.abs(err) - bound)
     assert np.all(np.abs(err) <= bound), \
         f"{what} |err| {np.abs(err).flat[worst]:.3e} at |ref| {np.abs(ref).flat[worst]:.3e}, rms {rms:.3e}"
@@ -196,7 +206,7 @@ def check_against_oracle_a16(cfg, res, hidden, logits, bias, W, map_rc, token_se
     mag = np.abs(w[sel].astype(np.float64)[:, :, None] * ypair.reshape(len(sel), k, cfg.H)).sum(1)
     bound = 2.0 ** -7 * mag + 2.0 ** -8 * np.abs(exp) + 1e-30
     assert np.all(np.abs(got - exp) <= bound), "GEMM2/combine off beyond bf16 rounding"
-    rel = assert_out_close_a16(res["out"][sel], ref["out"], "end to end")
+    rel = assert_out_close_a16(res["out"][sel], ref["out"], "end to end", pair_magnitude(ref, k))
     return rel, ref
 
 

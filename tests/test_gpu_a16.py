@@ -5,7 +5,7 @@ Bit-exact: routing, physical experts, recorded counts, segment offsets,
 dispatch order and the dispatched bf16 rows.  h in bf16: every element within
 one bf16 step of the oracle's, >= 99.5% identical.  GEMM2 + combine fed with
 the GPU's h: within bf16 rounding.  Layer output: relative L2 <= 4e-3 and
-every |err| within one bf16 step of the element plus 0.01 rms(out).
+every |err| within 2^-7 (|out| + sum_j |w_j y_j|) + 0.01 rms(out).
 """
 import dataclasses
 
@@ -112,8 +112,8 @@ def test_format_switch_and_route_rules(torch):
     run.act = mm.ACT_BF16
     a16 = run.forward(hidden, logits, bias)
     assert a16["status"] == 0
-    ref = oracle.forward(hidden, logits, bias, cfg.k, W, act="bf16")["out"]
-    gpu_util.assert_out_close_a16(a16["out"], ref)
+    ref = oracle.forward(hidden, logits, bias, cfg.k, W, act="bf16")
+    gpu_util.assert_out_close_a16(a16["out"], ref["out"], mag=gpu_util.pair_magnitude(ref, cfg.k))
     # stages 6 and 8 (activation scales) are empty in the bf16 format; 5 and 7 hold bf16 rows
     rows = int(a16["offsets"][-1])
     assert C_size(lib, h, 6) == 0 and C_size(lib, h, 8) == 0

@@ -32,10 +32,10 @@ def torch():
     return torch
 
 
-def _faulty_run(cfg, T, fault):
+def _faulty_run(cfg, T, fault, act=0):
     os.environ["MM_FAULT"] = fault
     try:
-        run = gpu_util.Run(cfg, cap=T)
+        run = gpu_util.Run(cfg, cap=T, act=act)
     finally:
         del os.environ["MM_FAULT"]
     hidden, logits, bias = synthetic.make_activations(cfg, T)
@@ -62,3 +62,20 @@ def test_injected_wait_times_out_and_context_survives(torch, fault, T, site, rou
     assert res["status"] == 0
     ref = oracle.forward(*inputs, cfg.k, gpu_util.weights(cfg))
     gpu_util.assert_out_close(res["out"], ref["out"])
+
+
+@pytest.mark.parametrize("T", [64, 1200])
+def test_injected_wait_times_out_in_the_a16w4_gemm(torch, T):
+    # the bf16 x MXFP4 GEMM's token producer waits for GEMM1 units that never come
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    status, took, got_site, inputs = _faulty_run(cfg, T, "gemm_dependency", act=mm.ACT_BF16)
+    assert took == 2
+    assert status == mm.MM_ERR_TIMEOUT
+    assert got_site == SITE_PRODUCER_DONE1
+    run = gpu_util.Run(cfg, cap=T, act=mm.ACT_BF16)
+    res = run.forward(*inputs, dumps=False)
+    run.close()
+    assert res["status"] == 0
+    ref = oracle.forward(*inputs, cfg.k, gpu_util.weights(cfg), act="bf16")
+    gpu_util.assert_out_close_a16(res["out"], ref["out"], mag=gpu_util.pair_magnitude(ref, cfg.k))
