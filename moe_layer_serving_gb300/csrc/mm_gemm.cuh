@@ -6,9 +6,10 @@
 // A = a token tile (e4m3, K-major, one e8m0 scale per 32), B = 256 rows of
 // MXFP4 weights (e2m1 unpacked to one byte per element in shared memory by the
 // TMA, K-major, one e8m0 scale per 32); tcgen05.mma kind::mxf8f6f4
-// block_scale, fp32 accumulators in tensor memory.  A block-scaled MMA takes
-// about the same time for any N, so N is always the full 256 (or 128 for a
-// ragged last block of GEMM2):
+// block_scale, fp32 accumulators in tensor memory.  An MMA costs at least ~45
+// cycles whatever its N and reaches the full rate only at N = 256 (128 cycles
+// for 128 x 256 x 32), so N is always the full 256 (or 128 for a ragged last
+// block of GEMM2):
 //
 //   GEMM1 unit (tile, n-block nb): B = gate rows [nb*128, +128) and up rows
 //       [I + nb*128, +128) of W1[p]; accumulator column c holds gate and
@@ -24,8 +25,9 @@
 // cheaper units take more of them (GEMM1 units stream 3.5x the weight bytes of
 // GEMM2 units, so a fixed round-robin split leaves some SMs a whole GEMM1 unit
 // behind).  All GEMM1 units precede all GEMM2 units, and a GEMM2 unit waits
-// (bounded) until the GEMM1 units of its tile have published hq.  Warp roles: 0 = TMA producer, 1 =
-// tensor-memory owner + MMA issuer, 2..9 = epilogue.  The eight epilogue warps
+// (bounded) until the GEMM1 units of its tile have published hq.  Warp roles:
+// 0 = TMA producer (one lane), 1 = tensor-memory owner + MMA issuer (the whole
+// warp, one elected lane issuing), 2..9 = epilogue.  The eight epilogue warps
 // first drain the accumulator into registers (each warp: its 32 token rows,
 // half of the columns) and release tensor memory, so the next unit's MMAs run
 // while they compute.
