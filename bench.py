@@ -75,6 +75,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the oracle's timed sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
+    ap.add_argument("--route", choices=["auto", "small", "large"], default="auto",
+                    help="path: auto (fused kernel up to 512 tokens), or force the fused or the multi-launch path")
     ap.add_argument("--act", choices=["mxfp8", "bf16"], default="mxfp8",
                     help="activation format: mxfp8 (a8w4, the fused operator) or bf16 (the a16w4 variant)")
     ap.add_argument("--experts", type=int, default=0,
@@ -82,9 +84,10 @@ def parse():
     return ap.parse_args()
 
 
-def workload_config(cfg, act="mxfp8"):
+def workload_config(cfg, act="mxfp8", route="auto"):
     name = "a8w4" if act == "mxfp8" else "a16w4"
-    return {"workload": f"moe-layer-{name}-T{cfg.T}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+    suffix = "" if route == "auto" else f"-{route}-path"
+    return {"workload": f"moe-layer-{name}-T{cfg.T}{suffix}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
             "P": cfg.P, "topk": cfg.k, "routing": "zipf" if cfg.zipf_s else "uniform",
             "eplb_redundant": cfg.P - cfg.E, "l2": "weights 6 GB > L2, no flush",
             "parallelism": "replicas"}
@@ -235,6 +238,7 @@ def main():
     a16 = args.act == "bf16"
     if a16:
         op.set_activation_format(mm.ACT_BF16)
+    op.set_route({"auto": mm.ROUTE_AUTO, "small": mm.ROUTE_SMALL, "large": mm.ROUTE_LARGE}[args.route])
     op.reserve(cfg.T)
     op.set_recording(cfg.recording)
     x = torch.from_numpy(hidden.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -308,7 +312,7 @@ def main():
     if os.path.exists(pk):
         peaks = json.load(open(pk))
     kname = "gemm16_kernel" if a16 else ("small_kernel" if route == 1 else "gemm_kernel")
-    wname = workload_config(cfg, args.act)["workload"]
+    wname = workload_config(cfg, args.act, args.route)["workload"]
     if cfg.T <= 512:
         alg = touched * expert_bytes(cfg)           # weight streaming: the touched experts' bytes
         achieved = alg / (kern_ms / 1e3) / 1e9
@@ -331,7 +335,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16xe2m1->f32" if a16 else "e4m3xe2m1->f32",
-        "data": "synthetic (seeded, random-init weights)", "config": workload_config(cfg, args.act), "clocks": clk, "gpu_launches": launches * args.steps,
+        "data": "synthetic (seeded, random-init weights)", "config": workload_config(cfg, args.act, args.route), "clocks": clk, "gpu_launches": launches * args.steps,
         "route": "small" if route == 1 else "large", "kernel_ms": kern_ms, "touched_experts": touched,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": roof,
