@@ -126,29 +126,53 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
     }
 }
 
-__global__ void __launch_bounds__(32) scatter_kernel(const int32_t* phys, int64_t npairs, int P,
-                                                     const int32_t* chunk_base, const int32_t* off, int32_t* pos)
+// Stable scatter of one chunk of (token, slot) pairs: eight warps take 128
+// consecutive pairs each, count them per expert, take exclusive prefixes of
+// those counts across warps (so a warp's pairs follow every earlier warp's in
+// each expert's segment), then place their pairs in order.
+constexpr int kScatterWarps = 8;
+static_assert(kChunkPairs % (32 * kScatterWarps) == 0, "a chunk splits evenly over the warps");
+
+__global__ void __launch_bounds__(32 * kScatterWarps) scatter_kernel(const int32_t* phys, int64_t npairs, int P,
+                                                                     const int32_t* chunk_base, const int32_t* off,
+                                                                     int32_t* pos)
 {
-    __shared__ int run[MM_MAX_EXPERTS];
-    const int lane = threadIdx.x;
-    for (int p = lane; p < P; p += 32) run[p] = 0;
-    __syncwarp();
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunkPairs;
-    const int32_t* cb = chunk_base + static_cast<int64_t>(blockIdx.x) * P;
+    __shared__ int wcnt[kScatterWarps][MM_MAX_EXPERTS];   // per-warp counts, then the warp's bases
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    constexpr int kPer = kChunkPairs / kScatterWarps;
+    for (int i = threadIdx.x; i < kScatterWarps * MM_MAX_EXPERTS; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunkPairs + w * kPer;
     const uint32_t lt = (1u << lane) - 1u;
-    for (int it = 0; it < kChunkPairs / 32; ++it) {
+    for (int it = 0; it < kPer / 32; ++it) {
         const int64_t i = base + it * 32 + lane;
-        if (base + it * 32 >= npairs) break;
-        const bool valid = i < npairs;
-        const int p = valid ? phys[i] : -1;
+        const int p = i < npairs ? phys[i] : -1;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
+        if (p >= 0 && lane == __ffs(peers) - 1) wcnt[w][p] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    const int32_t* cb = chunk_base + static_cast<int64_t>(blockIdx.x) * P;
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        int run = off[p] + cb[p];
+        for (int x = 0; x < kScatterWarps; ++x) {
+            const int v = wcnt[x][p];
+            wcnt[x][p] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int it = 0; it < kPer / 32; ++it) {
+        const int64_t i = base + it * 32 + lane;
+        const int p = i < npairs ? phys[i] : -1;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
         int before = 0;
-        if (valid) {
-            before = run[p];
-            pos[i] = off[p] + cb[p] + before + __popc(peers & lt);
+        if (p >= 0) {
+            before = wcnt[w][p];
+            pos[i] = before + __popc(peers & lt);
         }
         __syncwarp();
-        if (valid && lane == __ffs(peers) - 1) run[p] = before + __popc(peers);
+        if (p >= 0 && lane == __ffs(peers) - 1) wcnt[w][p] = before + __popc(peers);
         __syncwarp();
     }
 }
@@ -265,7 +289,7 @@ cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
     a.num_tiles = c->num_tiles;
     a.done1 = c->done1;
     scan_kernel<<<1, 512, 0, s>>>(a);
-    scatter_kernel<<<nchunks, 32, 0, s>>>(c->phys, npairs, c->P, c->chunk_hist, c->off, c->pos);
+    scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(c->phys, npairs, c->P, c->chunk_hist, c->off, c->pos);
     return cudaGetLastError();
 }
 
