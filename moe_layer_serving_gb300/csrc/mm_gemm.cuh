@@ -47,8 +47,11 @@ constexpr int kThreads = 320;              // 10 warps
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: accumulator [0, 256), then the current stage's scale factors
-constexpr uint32_t kColSFA = 256, kColSFB = 260;   // SFB: 4 columns per 128 weight rows
+// TMEM columns: accumulator [0, 256), then one scale-factor slot of 16 columns
+// per pipeline stage (SFA: 4 columns, SFB: 4 columns per 128 weight rows).  A
+// stage's copy into its own slot never waits for the MMAs of the stage before
+// it to have read their scales.
+constexpr uint32_t kColSF = 256, kSFSlotCols = 16, kColSFB = 4;
 
 // Shared-memory pipeline geometry: token rows held per stage (the tile size
 // of the kernel's token tiles) and the number of stages.  The MMA reads 128
@@ -357,7 +360,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, 
     static_assert(kKStep == 4 * 32, "four MMAs of K = 32 per stage");
     static_assert(kStages * G::kStageBytes + 1024 < (1 << 18), "descriptor address field");
     constexpr uint64_t kStageDesc = G::kStageBytes >> 4, kSfDesc = kSFBytes >> 4;
-    const uint32_t t_sfa = tmem + kColSFA, t_sfb = tmem + kColSFB;
+    static_assert(kColSF + kMaxStages * kSFSlotCols <= kTmemCols, "scale slots fit the allocation");
     const int lane = threadIdx.x & 31;
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -391,6 +394,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& g, const TileView& tv, 
             tc_fence_after();
             const uint64_t off = static_cast<uint64_t>(stage) * kStageDesc;
             const uint64_t ad = a_desc0 + off, bd = b_desc0 + off, sd = sf_desc0 + off;
+            const uint32_t t_sfa = tmem + kColSF + stage * kSFSlotCols, t_sfb = t_sfa + kColSFB;
             if (elect_one()) {
                 tc_cp_32x128b_x4(t_sfa, sd);
                 tc_cp_32x128b_x4(t_sfb, sd + kSfDesc);

@@ -96,11 +96,20 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
     const int p = threadIdx.x;
     int cnt = 0;
     if (p < a.P) {
-        for (int c = 0; c < a.nchunks; ++c) {
-            int32_t* h = a.chunk_hist + static_cast<int64_t>(c) * a.P + p;
-            const int v = *h;
-            *h = cnt;
-            cnt += v;
+        // exclusive prefix over the chunks of this expert's counts; each batch
+        // of loads is issued before its stores
+        constexpr int kBatch = 16;
+        int32_t* h = a.chunk_hist + p;
+        for (int c0 = 0; c0 < a.nchunks; c0 += kBatch) {
+            int v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                v[u] = c0 + u < a.nchunks ? h[static_cast<int64_t>(c0 + u) * a.P] : 0;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (c0 + u < a.nchunks) h[static_cast<int64_t>(c0 + u) * a.P] = cnt;
+                cnt += v[u];
+            }
         }
     }
     const int padded = seg_rows(cnt);

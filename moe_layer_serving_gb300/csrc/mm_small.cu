@@ -57,6 +57,53 @@ struct SmallArgs {
     int P;
 };
 
+// Exclusive scan over the block's threads of two ints (every thread calls it):
+// ea / eb = the sums of a / b over lower threads, ta / tb = the block totals.
+// wsum: 66 ints of shared scratch.
+__device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* wsum)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, ia, o);
+        const int y = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+        if (lane >= o) {
+            ia += x;
+            ib += y;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = ia;
+        wsum[32 + warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int x = lane < kSmallWarps ? wsum[lane] : 0, y = lane < kSmallWarps ? wsum[32 + lane] : 0;
+        int ix = x, iy = y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, ix, o);
+            const int v = __shfl_up_sync(0xFFFFFFFFu, iy, o);
+            if (lane >= o) {
+                ix += u;
+                iy += v;
+            }
+        }
+        wsum[lane] = ix - x;
+        wsum[32 + lane] = iy - y;
+        if (lane == 31) {
+            wsum[64] = ix;
+            wsum[65] = iy;
+        }
+    }
+    __syncthreads();
+    ea = wsum[warp] + ia - a;
+    eb = wsum[32 + warp] + ib - b;
+    ta = wsum[64];
+    tb = wsum[65];
+}
+
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
 {
     unsigned v;
@@ -129,12 +176,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* cnt = wcnt + kSmallWarps * MM_MAX_EXPERTS;          // [P]
     int* soff = cnt + MM_MAX_EXPERTS;                        // [P+1]
     int* stoff = soff + MM_MAX_EXPERTS + 1;                  // [P]
+    int* wsum = stoff + MM_MAX_EXPERTS;                      // [66] block-scan scratch
+    static_assert((2 * kMaxSmallPairs + (kSmallWarps + 3) * MM_MAX_EXPERTS + 1 + 66) * 4 <= kStageRegion,
+                  "permute scratch fits the pipeline buffers");
     const int chunk = ((N + kSmallWarps - 1) / kSmallWarps + 31) & ~31;
     bool short_tiles = true;
     const int lo = min(N, warp * chunk), hi = min(N, lo + chunk);
     const uint32_t lt = (1u << lane) - 1u;
     if (ok) {
-        for (int i = threadIdx.x; i < N; i += kThreads) sphys[i] = a.route.phys[i];
+        // the pairs' physical experts: each thread issues its loads before storing
+        for (int i0 = threadIdx.x; i0 < N; i0 += 8 * kThreads) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kThreads;
+                v[u] = i < N ? a.route.phys[i] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kThreads;
+                if (i < N) sphys[i] = v[u];
+            }
+        }
         for (int i = threadIdx.x; i < kSmallWarps * P; i += kThreads) wcnt[(i / P) * MM_MAX_EXPERTS + i % P] = 0;
         if (threadIdx.x < 2) scal[2 + threadIdx.x] = 0;
         __syncthreads();
@@ -164,36 +227,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // short tiles unless they would add more than 1/16 to the tile count
         short_tiles = 16 * scal[2] <= 17 * scal[3];
         const int tile = short_tiles ? kSmallTile : kTokTile;
-        if (warp == 0) {
-            // exclusive scans over experts of the padded segment sizes and tile counts
-            const int per = (P + 31) / 32;
-            const int p0 = lane * per, p1 = min(P, p0 + per);
+        {
+            // exclusive scans over experts of the padded segment sizes and tile
+            // counts: thread i takes experts [i * per, i * per + per)
+            const int per = (P + kThreads - 1) / kThreads;
+            const int p0 = min(P, static_cast<int>(threadIdx.x) * per), p1 = min(P, p0 + per);
             int rows = 0, tiles = 0;
             for (int p = p0; p < p1; ++p) {
                 rows += seg_rows(cnt[p]);
                 tiles += tiles_of(cnt[p], tile);
             }
-            int rx = rows, tx = tiles;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int r = __shfl_up_sync(0xFFFFFFFFu, rx, o);
-                const int q = __shfl_up_sync(0xFFFFFFFFu, tx, o);
-                if (lane >= o) {
-                    rx += r;
-                    tx += q;
-                }
-            }
-            int ro = rx - rows, to = tx - tiles;
+            int ro, to, rtot, ttot;
+            block_scan2(rows, tiles, ro, to, rtot, ttot, wsum);
             for (int p = p0; p < p1; ++p) {
                 soff[p] = ro;
                 stoff[p] = to;
                 ro += seg_rows(cnt[p]);
                 to += tiles_of(cnt[p], tile);
             }
-            if (lane == 31) {
-                soff[P] = rx;
-                scal[0] = tx;
-                scal[1] = rx;
+            if (threadIdx.x == 0) {
+                soff[P] = rtot;
+                scal[0] = ttot;
+                scal[1] = rtot;
             }
         }
         __syncthreads();
