@@ -73,7 +73,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the oracle's timed sample")
+    ap.add_argument("--cpu-sample", type=int, default=8, help="tokens per step in the reference arm's sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work the oracle baseline leg runs (its token sample doubles up to the batch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
     ap.add_argument("--route", choices=["auto", "small", "large"], default="auto",
                     help="path: auto (fused kernel up to 512 tokens), or force the fused or the multi-launch path")
@@ -147,6 +149,21 @@ def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens, act="mxfp8"
     oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel, act=act)
     dt = time.perf_counter() - t0
     return sel.size / dt, dt, sel.size
+
+
+def oracle_bounded_rate(cfg, hidden, logits, bias, W, pmap, seconds, act="mxfp8"):
+    """Tokens/s of the CPU oracle over about `seconds` of work: the token sample
+    doubles from 8 until one run takes a quarter of that or covers the batch,
+    then that sample runs until the time is spent (at most 8 runs)."""
+    n = min(8, cfg.T)
+    rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, act)
+    while dt < seconds / 4 and n < cfg.T:
+        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, min(2 * n, cfg.T), act)
+    toks, total, reps = n, dt, 1
+    while total < seconds and reps < 8:
+        _, d, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, act)
+        toks, total, reps = toks + n, total + d, reps + 1
+    return toks / total, total, n, reps
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -342,9 +359,9 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
-        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_sample, args.act)
+        rate, total, n, reps = oracle_bounded_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_seconds, args.act)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-                                "sample": f"first {n} of {cfg.T} tokens, all stages, {dt:.1f} s"}
+                                "sample": f"{reps} x first {n} of {cfg.T} tokens, all stages, {total:.1f} s timed"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     op.close()
