@@ -96,7 +96,8 @@ def workload_config(cfg, act="mxfp8", route="auto"):
 
 
 class ClockSampler:
-    """nvidia-smi samples of the SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (200 ms apart) of the SM clock and throttle reasons;
+    stop(since, until) keeps the samples taken between the two (time.monotonic())."""
 
     FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
@@ -120,9 +121,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) == 7:
-                self.rows.append(parts)
+                self.rows.append((time.monotonic(), parts))
 
-    def stop(self):
+    def stop(self, since=None, until=None):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -132,12 +133,16 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        rows = [r for t, r in self.rows if (since is None or t >= since) and (until is None or t <= until)]
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(rows)}
+
+
+SOAK_S = 1.0
 
 
 def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens, act="mxfp8"):
@@ -286,6 +291,7 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    t_load = time.monotonic()
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for i in range(args.steps):
@@ -293,7 +299,16 @@ def main():
         ev1.record(stream)
     stream.synchronize()
     kern = op.profile_end()
-    clk = clocks.stop()
+    # a short timed region falls between two clock samples: the same steps run on,
+    # untimed, for SOAK_S more seconds so that the clocks are sampled under this load
+    t_soak = time.monotonic()
+    with torch.cuda.stream(stream):
+        while time.monotonic() - t_soak < SOAK_S:
+            for i in range(args.steps):
+                op.forward(x, lg, b, out, stream=stream)
+            stream.synchronize()
+    clk = clocks.stop(since=t_load, until=time.monotonic())
+    clk["window"] = f"the timed steps and {SOAK_S:.0f} s more of them"
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
