@@ -73,7 +73,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-sample", type=int, default=8, help="tokens per step in the reference arm's sample")
+    ap.add_argument("--cpu-sample", type=int, default=64,
+                    help="tokens per step in the reference arm's sample (the oracle dequantises each touched "
+                         "expert once per call, so a whole decode batch is the representative sample)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work the oracle baseline leg runs (its token sample doubles up to the batch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
