@@ -93,6 +93,11 @@ def test_prefill_t8192(torch):
     _cfg(3, sample=16)
 
 
+def test_skewed_eplb_t16384(torch):
+    # skewed routing with 64 redundant replicas and the recorder on
+    _cfg(4, sample=16)
+
+
 def test_format_switch_and_route_rules(torch):
     import moe_layer_serving_gb300 as mm
     cfg = synthetic.CONFIGS[0]
