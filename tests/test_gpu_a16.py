@@ -82,7 +82,7 @@ def test_many_tiles_per_expert(torch):
 
 
 def test_decode_t64(torch):
-    _cfg(1, sample=24)
+    _cfg(1)                 # every token of the decode batch
 
 
 def test_eplb_t512(torch):

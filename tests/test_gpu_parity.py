@@ -5,8 +5,9 @@ segment offsets and dispatch order, MXFP8 activation codes and scales.
 GEMM1 requantised codes: >= 99.9% identical, the rest one e4m3 step apart.
 GEMM2 + combine fed with the GPU's hq: within bf16 rounding.
 Layer output: relative L2 <= 1e-2 and every |err| <= 0.05 rms(out).
-Full-size workloads compare sampled tokens end to end and all tokens for
-routing, remap, counts and dispatch.
+The decode batch is compared end to end on every token; the larger
+workloads compare sampled tokens end to end and all tokens for routing,
+remap, counts and dispatch.
 """
 import numpy as np
 import pytest
@@ -55,11 +56,11 @@ def test_config0_shapes_ragged_token_counts(T):
 
 
 def test_config1_decode_t64():
-    _cfg_run(1, sample=24)
+    _cfg_run(1)             # every token of the decode batch
 
 
 def test_config2_eplb_t512():
-    _cfg_run(2, sample=24)
+    _cfg_run(2, sample=128)
 
 
 def test_config3_prefill_t8192():
