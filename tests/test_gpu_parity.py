@@ -116,3 +116,24 @@ def test_concentrated_routing_many_tiles_per_expert(T):
     assert res["status"] == 0
     assert np.all(np.sort(res["idx"], axis=1) == np.arange(8))
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(T, 40))
+
+
+@pytest.mark.parametrize("T,E,route", [(37, 1, 1), (1100, 1, 2), (300, 8, 1)])
+def test_top1_degenerate_routing(T, E, route):
+    # top-1: every weight is 1.0; with one expert the layer is a dense SwiGLU
+    # MLP over all tokens (one segment of T rows: one tile in the fused
+    # kernel at T = 37, nine 128-row tiles on the large path at T = 1100)
+    import dataclasses
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T, E=E, P=E, k=1)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    W = synthetic.make_all_weights(cfg)
+    run = gpu_util.Run(cfg, W, cap=T)
+    res = run.forward(hidden, logits, bias)
+    info = run.op.last_info()
+    run.close()
+    assert res["status"] == 0
+    assert info[0] == route
+    assert np.all(res["weights"] == 1.0)
+    if E == 1:
+        assert np.all(res["idx"] == 0)
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None)
