@@ -137,3 +137,37 @@ def test_top1_degenerate_routing(T, E, route):
     if E == 1:
         assert np.all(res["idx"] == 0)
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None)
+
+
+@pytest.mark.parametrize("route", [1, 2])
+def test_special_values_and_routing_ties(route):
+    # token rows that are all zero, hold a zero 32-block, or sit far from unit
+    # scale; logits that tie across all experts (top-k = the lowest indices) or
+    # between the two best; both paths (fused kernel, large path)
+    import dataclasses
+    import moe_layer_serving_gb300 as mm
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=40)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    x = synthetic.f32_from_bf16_bits(hidden)
+    x[0] = 0.0
+    x[1, :32] = 0.0
+    x[2] *= 1.0e4
+    x[3] *= 1.0e-6
+    hidden = synthetic.bf16_bits_from_f32(x)
+    logits[5] = 0.25
+    logits[6, 3] = logits[6, 6] = logits[6].max() + 1.0
+    W = synthetic.make_all_weights(cfg)
+    run = gpu_util.Run(cfg, W, cap=cfg.T)
+    run.op.set_route(mm.ROUTE_SMALL if route == 1 else mm.ROUTE_LARGE)
+    res = run.forward(hidden, logits, bias)
+    assert run.op.last_info()[0] == route
+    run.close()
+    assert res["status"] == 0
+    assert list(res["idx"][5]) == list(range(cfg.k))
+    assert list(res["idx"][6][:2]) == [3, 6]
+    assert not np.any(synthetic.f32_from_bf16_bits(res["out"][0]))      # a zero token gives a zero output
+    # the row scaled by 1e4 has outputs ~1e6 and would set the rms of the whole
+    # batch: each magnitude regime is held to the tolerance against its own rms
+    rest = np.array([t for t in range(cfg.T) if t != 2])
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, rest)
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, np.array([2]))
