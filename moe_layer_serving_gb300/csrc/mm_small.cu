@@ -104,33 +104,40 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int&
     tb = wsum[65];
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
 {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Sense-counting grid barrier: the last CTA to arrive resets the count and
-// bumps the generation; the others wait (bounded) for the bump.
+// Counting grid barrier over a 64-bit arrival count that only grows: every
+// barrier adds exactly gridDim.x arrivals, so between barriers the count is a
+// multiple of the grid, and a CTA whose arrival returned `old` waits (bounded)
+// until the count reaches the next multiple above it.  The last CTA to arrive
+// releases everyone with its own arrival: no reset, no second word.  (The host
+// zeroes the count after a device error, when arrivals may be missing.)
 __device__ bool grid_sync(unsigned* bar, int* status, volatile int* abort_flag, bool withhold = false)
 {
     __syncthreads();
     if (threadIdx.x == 0 && !*abort_flag) {
-        const unsigned gen = ld_acquire_u32(bar + 1);
+        unsigned long long* cnt = reinterpret_cast<unsigned long long*>(bar);
+        const unsigned long long G = gridDim.x;
         __threadfence();
-        if (!withhold && atomicAdd(bar, 1u) + 1u == gridDim.x) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
+        unsigned long long target;
+        if (!withhold) {
+            const unsigned long long old = atomicAdd(cnt, 1ull);
+            target = old - old % G + G;
         } else {
-            const uint64_t t0 = globaltimer();
-            while (ld_acquire_u32(bar + 1) == gen) {
-                if (globaltimer() - t0 > kWaitLimitNs) {
-                    latch_error(status, MM_ERR_TIMEOUT, kSiteGridBarrier);
-                    *abort_flag = 1;
-                    break;
-                }
+            const unsigned long long cur = ld_acquire_u64(cnt);
+            target = cur - cur % G + G;
+        }
+        const uint64_t t0 = globaltimer();
+        while (ld_acquire_u64(cnt) < target) {
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                latch_error(status, MM_ERR_TIMEOUT, kSiteGridBarrier);
+                *abort_flag = 1;
+                break;
             }
         }
         __threadfence();
