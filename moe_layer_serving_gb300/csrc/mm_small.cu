@@ -57,51 +57,50 @@ struct SmallArgs {
     int P;
 };
 
-// Exclusive scan over the block's threads of two ints (every thread calls it):
-// ea / eb = the sums of a / b over lower threads, ta / tb = the block totals.
-// wsum: 66 ints of shared scratch.
-__device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* wsum)
+// Exclusive scan over the block's threads of three ints (every thread calls
+// it): e[i] = the sum of v[i] over lower threads, t[i] = the block total.
+// wsum: 99 ints of shared scratch.
+constexpr int kScanVals = 3;
+__device__ __forceinline__ void block_scan3(const int (&v)[kScanVals], int (&e)[kScanVals], int (&t)[kScanVals],
+                                            int* wsum)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int ia = a, ib = b;
+    int in[kScanVals];
+#pragma unroll
+    for (int i = 0; i < kScanVals; ++i) in[i] = v[i];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xFFFFFFFFu, ia, o);
-        const int y = __shfl_up_sync(0xFFFFFFFFu, ib, o);
-        if (lane >= o) {
-            ia += x;
-            ib += y;
+#pragma unroll
+        for (int i = 0; i < kScanVals; ++i) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, in[i], o);
+            if (lane >= o) in[i] += x;
         }
     }
     if (lane == 31) {
-        wsum[warp] = ia;
-        wsum[32 + warp] = ib;
+#pragma unroll
+        for (int i = 0; i < kScanVals; ++i) wsum[32 * i + warp] = in[i];
     }
     __syncthreads();
     if (warp == 0) {
-        const int x = lane < kSmallWarps ? wsum[lane] : 0, y = lane < kSmallWarps ? wsum[32 + lane] : 0;
-        int ix = x, iy = y;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xFFFFFFFFu, ix, o);
-            const int v = __shfl_up_sync(0xFFFFFFFFu, iy, o);
-            if (lane >= o) {
-                ix += u;
-                iy += v;
+        for (int i = 0; i < kScanVals; ++i) {
+            const int x = lane < kSmallWarps ? wsum[32 * i + lane] : 0;
+            int ix = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xFFFFFFFFu, ix, o);
+                if (lane >= o) ix += u;
             }
-        }
-        wsum[lane] = ix - x;
-        wsum[32 + lane] = iy - y;
-        if (lane == 31) {
-            wsum[64] = ix;
-            wsum[65] = iy;
+            wsum[32 * i + lane] = ix - x;
+            if (lane == 31) wsum[96 + i] = ix;
         }
     }
     __syncthreads();
-    ea = wsum[warp] + ia - a;
-    eb = wsum[32 + warp] + ib - b;
-    ta = wsum[64];
-    tb = wsum[65];
+#pragma unroll
+    for (int i = 0; i < kScanVals; ++i) {
+        e[i] = wsum[32 * i + warp] + in[i] - v[i];
+        t[i] = wsum[96 + i];
+    }
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
@@ -183,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* cnt = wcnt + kSmallWarps * MM_MAX_EXPERTS;          // [P]
     int* soff = cnt + MM_MAX_EXPERTS;                        // [P+1]
     int* stoff = soff + MM_MAX_EXPERTS + 1;                  // [P]
-    int* wsum = stoff + MM_MAX_EXPERTS;                      // [66] block-scan scratch
-    static_assert((2 * kMaxSmallPairs + (kSmallWarps + 3) * MM_MAX_EXPERTS + 1 + 66) * 4 <= kStageRegion,
+    int* wsum = stoff + MM_MAX_EXPERTS;                      // [99] block-scan scratch
+    static_assert((2 * kMaxSmallPairs + (kSmallWarps + 3) * MM_MAX_EXPERTS + 1 + 99) * 4 <= kStageRegion,
                   "permute scratch fits the pipeline buffers");
     const int chunk = ((N + kSmallWarps - 1) / kSmallWarps + 31) & ~31;
     bool short_tiles = true;
@@ -205,8 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i < N) sphys[i] = v[u];
             }
         }
-        for (int i = threadIdx.x; i < kSmallWarps * P; i += kThreads) wcnt[(i / P) * MM_MAX_EXPERTS + i % P] = 0;
-        if (threadIdx.x < 2) scal[2 + threadIdx.x] = 0;
+        for (int i = threadIdx.x; i < kSmallWarps * MM_MAX_EXPERTS; i += kThreads) wcnt[i] = 0;
         __syncthreads();
         int* wc = wcnt + warp * MM_MAX_EXPERTS;
         for (int base = lo; base < hi; base += 32) {
@@ -225,27 +223,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 run += v;
             }
             cnt[p] = run;
-            if (run > 0) {
-                atomicAdd(&scal[2], tiles_of(run, kSmallTile));
-                atomicAdd(&scal[3], tiles_of(run, kTokTile));
-            }
         }
         __syncthreads();
-        // short tiles unless they would add more than 1/16 to the tile count
-        short_tiles = 16 * scal[2] <= 17 * scal[3];
-        const int tile = short_tiles ? kSmallTile : kTokTile;
+        int tile;
         {
-            // exclusive scans over experts of the padded segment sizes and tile
-            // counts: thread i takes experts [i * per, i * per + per)
+            // exclusive scans over experts of the padded segment sizes and of the
+            // tile counts in both tile sizes (thread i takes experts [i * per,
+            // i * per + per)); the totals choose the tile size: short tiles
+            // unless they would add more than 1/16 to the tile count
             const int per = (P + kThreads - 1) / kThreads;
             const int p0 = min(P, static_cast<int>(threadIdx.x) * per), p1 = min(P, p0 + per);
-            int rows = 0, tiles = 0;
+            int v[kScanVals] = {0, 0, 0};
             for (int p = p0; p < p1; ++p) {
-                rows += seg_rows(cnt[p]);
-                tiles += tiles_of(cnt[p], tile);
+                v[0] += seg_rows(cnt[p]);
+                v[1] += tiles_of(cnt[p], kSmallTile);
+                v[2] += tiles_of(cnt[p], kTokTile);
             }
-            int ro, to, rtot, ttot;
-            block_scan2(rows, tiles, ro, to, rtot, ttot, wsum);
+            int e[kScanVals], tot[kScanVals];
+            block_scan3(v, e, tot, wsum);
+            short_tiles = 16 * tot[1] <= 17 * tot[2];
+            tile = short_tiles ? kSmallTile : kTokTile;
+            int ro = e[0], to = short_tiles ? e[1] : e[2];
             for (int p = p0; p < p1; ++p) {
                 soff[p] = ro;
                 stoff[p] = to;
@@ -253,9 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 to += tiles_of(cnt[p], tile);
             }
             if (threadIdx.x == 0) {
-                soff[P] = rtot;
-                scal[0] = ttot;
-                scal[1] = rtot;
+                soff[P] = tot[0];
+                scal[0] = short_tiles ? tot[1] : tot[2];
+                scal[1] = tot[0];
+                scal[2] = tot[1];
+                scal[3] = tot[2];
             }
         }
         __syncthreads();
