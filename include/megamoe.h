@@ -173,7 +173,10 @@ MM_API mm_status mm_read_counts(mm_handle h, int layer, int64_t *out_host);
 MM_API mm_status mm_reset_counts(mm_handle h, int layer);
 
 /* Synchronise the device, store the latched device status in *device_code
- * (0 = none, else an mm_status value) and clear it. */
+ * (0 = none, else an mm_status value) and clear it.  After a device error it
+ * also resets the fused kernel's grid-barrier count (an aborted launch may
+ * have left arrivals missing), so call it before the next forward once a
+ * forward has failed on the device. */
 MM_API mm_status mm_get_status(mm_handle h, int *device_code);
 
 /* Intermediates of the last forward, for tests.  Synchronous.  `stage`:
