@@ -34,8 +34,34 @@ METRIC = "MoE-layer tokens/s"
 EXPERT_BYTES_PER_ELEM = 0.5 + 1.0 / 32      # packed e2m1 + one e8m0 byte per 32
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its // and /* */ comments (string and character
+    literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def sources_digest() -> str:
-    """sha256 over the kernel sources (csrc/*.cu, *.cuh, *.h and the C header)."""
+    """sha256 over the kernel sources (csrc/*.cu, *.cuh, *.h and the C header)
+    with their comments removed: a comment edit does not change a kernel."""
     import hashlib
     csrc = os.path.join(ROOT, "moe_layer_serving_gb300", "csrc")
     files = sorted(os.path.join("moe_layer_serving_gb300", "csrc", f) for f in os.listdir(csrc)
@@ -44,8 +70,8 @@ def sources_digest() -> str:
     h = hashlib.sha256()
     for f in files:
         h.update(f.encode())
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(strip_c_comments(fh.read()).encode())
     return h.hexdigest()
 
 
