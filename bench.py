@@ -35,9 +35,15 @@ EXPERT_BYTES_PER_ELEM = 0.5 + 1.0 / 32      # packed e2m1 + one e8m0 byte per 32
 
 
 def strip_c_comments(text: str) -> str:
-    """C/C++ source without its // and /* */ comments (string and character
-    literals kept as they are)."""
+    """C/C++ source without its // and /* */ comments and with every run of
+    whitespace outside string and character literals made one space (the
+    literals are kept as they are)."""
     out, i, n = [], 0, len(text)
+
+    def space():
+        if out and out[-1] != " ":
+            out.append(" ")
+
     while i < n:
         c = text[i]
         if c in "\"'":
@@ -51,17 +57,21 @@ def strip_c_comments(text: str) -> str:
             i = n if j < 0 else j
         elif text.startswith("/*", i):
             j = text.find("*/", i + 2)
-            out.append(" ")
+            space()
             i = n if j < 0 else j + 2
+        elif c.isspace():
+            space()
+            i += 1
         else:
             out.append(c)
             i += 1
-    return "".join(out)
+    return "".join(out).strip()
 
 
 def sources_digest() -> str:
     """sha256 over the kernel sources (csrc/*.cu, *.cuh, *.h and the C header)
-    with their comments removed: a comment edit does not change a kernel."""
+    with comments removed and whitespace collapsed: editing a comment or the
+    layout does not change a kernel."""
     import hashlib
     csrc = os.path.join(ROOT, "moe_layer_serving_gb300", "csrc")
     files = sorted(os.path.join("moe_layer_serving_gb300", "csrc", f) for f in os.listdir(csrc)
