@@ -134,6 +134,7 @@ class MegaMoE:
     """One fused MoE layer operator (one handle) on the current CUDA device."""
 
     def __init__(self, num_experts: int, num_physical: int, topk: int, hidden: int, inter: int):
+        """E logical and P physical experts, top-k, hidden size H and expert inter size I (mm_create)."""
         h = C.c_void_p()
         _check(lib().mm_create(num_experts, num_physical, topk, hidden, inter, C.byref(h)), "mm_create")
         self._h = h
@@ -144,6 +145,7 @@ class MegaMoE:
         return self._h
 
     def close(self) -> None:
+        """Free the handle and its device memory (mm_destroy); idempotent."""
         if self._h:
             lib().mm_destroy(self._h)
             self._h = None
@@ -155,10 +157,14 @@ class MegaMoE:
             pass
 
     def set_weights(self, w1, w1_scale, w2, w2_scale) -> None:
+        """Device MXFP4 weights of the P physical experts: w1 [P, 2I, H/2] with scales
+        [P, 2I, H/32] (gate rows, then up rows), w2 [P, H, I/2] with scales [P, H, I/32];
+        copied into the library's tiled layout (mm_set_weights, synchronous)."""
         _check(lib().mm_set_weights(self._h, _addr(w1), _addr(w1_scale), _addr(w2), _addr(w2_scale)),
                "mm_set_weights")
 
     def set_eplb_map(self, phys_of_logical, replica_counts) -> None:
+        """Host arrays: physical ids [E, max_replicas] and replica counts [E] (mm_set_eplb_map)."""
         m = np.ascontiguousarray(phys_of_logical, np.int32)
         rc = np.ascontiguousarray(replica_counts, np.int32)
         _check(lib().mm_set_eplb_map(self._h, m.ctypes.data, rc.ctypes.data, m.shape[1]), "mm_set_eplb_map")
@@ -168,12 +174,15 @@ class MegaMoE:
         _check(lib().mm_rebalance(self._h, layer, max_replicas), "mm_rebalance")
 
     def bind_layer(self, layer: int) -> None:
+        """Count slot that later forwards record into (mm_bind_layer)."""
         _check(lib().mm_bind_layer(self._h, layer), "mm_bind_layer")
 
     def set_recording(self, on: bool) -> None:
+        """Record per-logical-expert token counts in forwards (mm_set_recording)."""
         _check(lib().mm_set_recording(self._h, int(bool(on))), "mm_set_recording")
 
     def set_route(self, route: int) -> None:
+        """ROUTE_AUTO, ROUTE_SMALL (fused kernel) or ROUTE_LARGE (multi-launch path)."""
         _check(lib().mm_set_route(self._h, route), "mm_set_route")
 
     def set_activation_format(self, act: int) -> None:
@@ -181,6 +190,7 @@ class MegaMoE:
         _check(lib().mm_set_activation_format(self._h, act), "mm_set_activation_format")
 
     def reserve(self, max_tokens: int) -> None:
+        """Allocate the workspace for up to max_tokens tokens per forward (mm_reserve)."""
         _check(lib().mm_reserve(self._h, max_tokens), "mm_reserve")
 
     def forward(self, hidden, logits, bias, out, num_tokens: int | None = None, stream=None) -> int:
@@ -191,14 +201,17 @@ class MegaMoE:
         return st
 
     def read_counts(self, layer: int) -> np.ndarray:
+        """int64 counts [E] of slot `layer` (synchronises; mm_read_counts)."""
         out = np.zeros(self.E, np.int64)
         _check(lib().mm_read_counts(self._h, layer, out.ctypes.data), "mm_read_counts")
         return out
 
     def reset_counts(self, layer: int = -1) -> None:
+        """Zero slot `layer`'s counts, or every slot's with -1 (mm_reset_counts)."""
         _check(lib().mm_reset_counts(self._h, layer), "mm_reset_counts")
 
     def get_status(self) -> int:
+        """Latched device status of earlier forwards (0 = none), cleared by the read (mm_get_status)."""
         code = C.c_int(0)
         _check(lib().mm_get_status(self._h, C.byref(code)), "mm_get_status")
         return code.value
@@ -221,6 +234,7 @@ class MegaMoE:
         return int(a[0]), int(a[1]), int(a[2])
 
     def debug_dump(self, stage: int) -> np.ndarray:
+        """Intermediate `stage` of the last forward as a flat array (see DUMP_STAGES)."""
         n = C.c_size_t(0)
         _check(lib().mm_debug_size(self._h, stage, C.byref(n)), "mm_debug_size")
         dtype = DUMP_STAGES[stage][1]
