@@ -221,6 +221,22 @@ def expert_ffn_a16(x, w1, w1s, w2, w2s, want_g=False):
     return out
 
 
+def append_shared(idx, w, phys, E, P, shared):
+    """Fused shared experts ("sglang PR #35619", settings that silently break it:
+    fusion sizes the operator with top-k plus the shared experts): every token
+    gets `shared` more slots after its k routed ones; slot k + s holds shared
+    expert s, logical id E + s (outside the routed experts, so the recorder
+    never counts it), weight 1 (its output is added as is) and physical id
+    P + s (after the P routed physical experts).  Reading: the pages give the
+    slot count only; weight 1 is the plain sum of a shared expert's output."""
+    T = idx.shape[0]
+    s = np.arange(shared, dtype=np.int32)
+    idx = np.concatenate([idx, np.broadcast_to(E + s, (T, shared))], axis=1).astype(np.int32)
+    w = np.concatenate([w, np.ones((T, shared), np.float32)], axis=1)
+    phys = np.concatenate([phys, np.broadcast_to(P + s, (T, shared))], axis=1).astype(np.int32)
+    return np.ascontiguousarray(idx), np.ascontiguousarray(w), np.ascontiguousarray(phys)
+
+
 def combine(w, ypair):
     """w [T,k] f32, ypair [T*k, H] f32 in pair order -> bf16 bits [T,H]"""
     w = _c(w, np.float32)
@@ -233,19 +249,21 @@ def combine(w, ypair):
 
 
 def forward(hidden, logits, bias, k, weights, phys_of_logical=None, replica_counts=None,
-            token_ids=None, want_g=False, act="mxfp8"):
+            token_ids=None, want_g=False, act="mxfp8", shared=0):
     """The whole layer for the given tokens.
 
     hidden bf16 bits [n,H], logits [n,E] for tokens ``token_ids`` (their index
     in the forward call; default 0..n-1).  weights = (w1, w1s, w2, w2s) indexed
     by physical expert.  ``act``: "mxfp8" (a8w4: activations quantised to
     MXFP8 before each GEMM) or "bf16" (a16w4: bf16 activations, h rounded to
-    bf16).  Returns a dict of every intermediate (pair order is (token, slot))
-    plus ``out`` (bf16 bits [n,H]) and ``counts`` (int64 [E]).
+    bf16).  ``shared``: fused shared experts, the last ``shared`` physical
+    experts of ``weights`` (see append_shared).  Returns a dict of every
+    intermediate (pair order is (token, slot)) plus ``out`` (bf16 bits [n,H])
+    and ``counts`` (int64 [E]).
     """
     if act == "bf16":
         return _forward_a16(hidden, logits, bias, k, weights, phys_of_logical, replica_counts,
-                            token_ids, want_g)
+                            token_ids, want_g, shared)
     assert act == "mxfp8", act
     w1, w1s, w2, w2s = weights
     n, H = hidden.shape
@@ -257,6 +275,9 @@ def forward(hidden, logits, bias, k, weights, phys_of_logical=None, replica_coun
     idx, w = route(logits, bias, k)
     phys = eplb(idx, phys_of_logical, replica_counts, token_ids)
     counts = record(idx, E)
+    if shared:
+        idx, w, phys = append_shared(idx, w, phys, E, P - shared, shared)
+    k += shared                       # slots per token from here on
     xq, xs = mxfp8_quant_bf16(hidden)
     off, order, pos = permute(phys, P)
     I = w2.shape[2] * 2
@@ -284,7 +305,7 @@ def forward(hidden, logits, bias, k, weights, phys_of_logical=None, replica_coun
 
 
 def _forward_a16(hidden, logits, bias, k, weights, phys_of_logical, replica_counts, token_ids,
-                 want_g):
+                 want_g, shared=0):
     w1, w1s, w2, w2s = weights
     n, H = hidden.shape
     E = logits.shape[1]
@@ -295,6 +316,9 @@ def _forward_a16(hidden, logits, bias, k, weights, phys_of_logical, replica_coun
     idx, w = route(logits, bias, k)
     phys = eplb(idx, phys_of_logical, replica_counts, token_ids)
     counts = record(idx, E)
+    if shared:
+        idx, w, phys = append_shared(idx, w, phys, E, P - shared, shared)
+    k += shared
     off, order, pos = permute(phys, P)
     I = w2.shape[2] * 2
     npairs = n * k

@@ -228,3 +228,50 @@ def test_zipf_workload_replicates_the_hottest_experts():
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
     hot = set(np.argsort(-counts, kind="stable")[:64].tolist())
     assert len(hot & set(range(64))) >= 56        # replicas sit on the popular experts
+
+
+# ---- fused shared experts ----------------------------------------------------
+def _shared_case(ns=1, T=24):
+    # E routed experts plus ns shared ones: the shared experts' weights are the
+    # last ns of E + ns independently drawn experts
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T, E=8, P=8, k=2)
+    wide = dataclasses.replace(cfg, E=cfg.E + ns, P=cfg.P + ns)
+    W = synthetic.make_all_weights(wide)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    return cfg, W, hidden, logits, bias
+
+
+@pytest.mark.parametrize("act", ["mxfp8", "bf16"])
+def test_shared_slots_leave_the_routed_part_alone(act):
+    cfg, W, hidden, logits, bias = _shared_case(ns=2)
+    base = oracle.forward(hidden, logits, bias, cfg.k, tuple(a[:cfg.P] for a in W), act=act)
+    res = oracle.forward(hidden, logits, bias, cfg.k, W, act=act, shared=2)
+    k = cfg.k
+    assert np.array_equal(res["idx"][:, :k], base["idx"]) and np.array_equal(res["w"][:, :k], base["w"])
+    assert np.array_equal(res["phys"][:, :k], base["phys"]) and np.array_equal(res["counts"], base["counts"])
+    assert np.all(res["idx"][:, k:] == cfg.E + np.arange(2)) and np.all(res["w"][:, k:] == 1.0)
+    assert np.all(res["phys"][:, k:] == cfg.P + np.arange(2))
+
+
+def test_shared_expert_alone_is_its_dense_ffn():
+    # routed down projections all zero: every routed y is exactly 0, so the
+    # layer output is the shared expert's own output for each token, computed
+    # here per token straight from the expert FFN (no permute, no combine)
+    cfg, W, hidden, logits, bias = _shared_case(ns=1)
+    w1, w1s, w2, w2s = (a.copy() for a in W)
+    w2[:cfg.P] = 0
+    res = oracle.forward(hidden, logits, bias, cfg.k, (w1, w1s, w2, w2s), shared=1)
+    xq, xs = oracle.mxfp8_quant_bf16(hidden)
+    y = oracle.expert_ffn(xq, xs, w1[cfg.P], w1s[cfg.P], w2[cfg.P], w2s[cfg.P])["y"]
+    assert np.any(y != 0)
+    assert np.array_equal(res["out"], synthetic.bf16_bits_from_f32(y))
+
+
+def test_shared_expert_alone_is_its_dense_ffn_a16():
+    cfg, W, hidden, logits, bias = _shared_case(ns=1)
+    w1, w1s, w2, w2s = (a.copy() for a in W)
+    w2[:cfg.P] = 0
+    res = oracle.forward(hidden, logits, bias, cfg.k, (w1, w1s, w2, w2s), act="bf16", shared=1)
+    y = oracle.expert_ffn_a16(hidden, w1[cfg.P], w1s[cfg.P], w2[cfg.P], w2s[cfg.P])["y"]
+    assert np.any(y != 0)
+    assert np.array_equal(res["out"], synthetic.bf16_bits_from_f32(y))
