@@ -99,9 +99,10 @@ MM_API mm_status mm_destroy(mm_handle h);
  *   w1_scale [P, 2I, H/32] e8m0
  *   w2       [P, H, I/2]   MXFP4 elements
  *   w2_scale [P, H, I/32]  e8m0
- * Copied (scales re-laid out for the tensor cores) into library-owned
- * memory; the caller may free its buffers after return.  Synchronous.  Not
- * allowed during stream capture. */
+ * (P + S experts when S fused shared experts are set, see
+ * mm_set_shared_experts.)  Copied (scales re-laid out for the tensor cores)
+ * into library-owned memory; the caller may free its buffers after return.
+ * Synchronous.  Not allowed during stream capture. */
 MM_API mm_status mm_set_weights(mm_handle h, const uint8_t *w1, const uint8_t *w1_scale,
                          const uint8_t *w2, const uint8_t *w2_scale);
 
@@ -143,6 +144,18 @@ MM_API mm_status mm_set_route(mm_handle h, mm_route route);
  * workspace (call mm_reserve again before forwarding).  Synchronous; not
  * allowed during stream capture.  An unknown value -> MM_ERR_INVALID_ARG. */
 MM_API mm_status mm_set_activation_format(mm_handle h, mm_act act);
+
+/* Fused shared experts ("sglang PR #35619", settings that silently break it:
+ * fusion sizes the operator with top-k plus the number of fused shared
+ * experts).  With num_shared = S > 0 every token gets S slots after its k
+ * routed ones: slot k + s is shared expert s, physical expert P + s, weight 1
+ * (its output is added as is), logical id E + s in the idx intermediate, never
+ * counted by the recorder.  mm_set_weights then takes P + S experts (the
+ * routed physical experts, then the shared ones); the EPLB map still covers the
+ * P routed ones.  Changing S drops the weights and the workspace (set them
+ * again).  0 <= S, k + S <= MM_MAX_TOPK, P + S <= MM_MAX_EXPERTS, else
+ * MM_ERR_INVALID_ARG.  Synchronous; not allowed during stream capture. */
+MM_API mm_status mm_set_shared_experts(mm_handle h, int num_shared);
 
 /* Reserve workspace for up to max_tokens tokens per forward (the pages' MTPR
  * capacity).  Allocates; call before any stream capture.  Calling again with

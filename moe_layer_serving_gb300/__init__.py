@@ -41,6 +41,7 @@ _SIGS = {
     "mm_set_recording": [_p, _i32],
     "mm_set_route": [_p, _i32],
     "mm_set_activation_format": [_p, _i32],
+    "mm_set_shared_experts": [_p, _i32],
     "mm_reserve": [_p, _i64],
     "mm_forward": [_p, _p, _p, _p, _p, _i64, _p],
     "mm_read_counts": [_p, _i32, _p],
@@ -139,6 +140,7 @@ class MegaMoE:
         _check(lib().mm_create(num_experts, num_physical, topk, hidden, inter, C.byref(h)), "mm_create")
         self._h = h
         self.E, self.P, self.k, self.H, self.I = num_experts, num_physical, topk, hidden, inter
+        self.S = 0
 
     @property
     def handle(self):
@@ -188,6 +190,12 @@ class MegaMoE:
     def set_activation_format(self, act: int) -> None:
         """ACT_MXFP8 (a8w4) or ACT_BF16 (a16w4); drops the workspace (reserve again)."""
         _check(lib().mm_set_activation_format(self._h, act), "mm_set_activation_format")
+
+    def set_shared_experts(self, num_shared: int) -> None:
+        """Fused shared experts: every token also goes to physical experts P .. P+S-1
+        with weight 1; drops the weights and the workspace (mm_set_shared_experts)."""
+        _check(lib().mm_set_shared_experts(self._h, num_shared), "mm_set_shared_experts")
+        self.S = num_shared
 
     def reserve(self, max_tokens: int) -> None:
         """Allocate the workspace for up to max_tokens tokens per forward (mm_reserve)."""

@@ -210,9 +210,9 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
     if (!c || !w1 || !w1s || !w2 || !w2s) return MM_ERR_INVALID_ARG;
     if (!aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1s, 16) || !aligned(w2s, 16)) return MM_ERR_INVALID_ARG;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
-    const size_t P = c->P, H = c->H, I = c->I;
+    const size_t P = mm::pw(c), H = c->H, I = c->I;      // routed and shared physical experts
     const mm::WOrder o1 = mm::w1_order(c->H, c->I), o2 = mm::w2_order(c->H, c->I);
-    const size_t b1 = mm::w_blocks(o1, c->P), b2 = mm::w_blocks(o2, c->P);
+    const size_t b1 = mm::w_blocks(o1, static_cast<int>(P)), b2 = mm::w_blocks(o2, static_cast<int>(P));
     const size_t n_w1 = b1 * 8192, n_w1s = b1 * 512;
     const size_t n_w2 = b2 * 8192, n_w2s = b2 * 512;
     if (!c->w1) {
@@ -380,17 +380,40 @@ mm_status mm_set_activation_format(mm_handle c, mm_act act)
     return MM_OK;
 }
 
+mm_status mm_set_shared_experts(mm_handle c, int num_shared)
+{
+    if (!c || num_shared < 0 || c->k + num_shared > MM_MAX_TOPK || c->P + num_shared > MM_MAX_EXPERTS)
+        return MM_ERR_INVALID_ARG;
+    if (num_shared == c->ns) return MM_OK;
+    if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    cudaDeviceSynchronize();
+    // every per-expert and per-pair size changes: weights and workspace go
+    free_ws(c);
+    c->cap_tokens = 0;
+    c->maps_ws = false;
+    cudaFree(c->w1);
+    cudaFree(c->w1_sf);
+    cudaFree(c->w2);
+    cudaFree(c->w2_sf);
+    c->w1 = c->w2 = c->w1_sf = c->w2_sf = nullptr;
+    c->weights_set = false;
+    c->maps_weights = false;
+    c->ns = num_shared;
+    return MM_OK;
+}
+
 mm_status mm_reserve(mm_handle c, int64_t max_tokens)
 {
     if (!c || max_tokens < 0 || max_tokens > (int64_t(1) << 24)) return MM_ERR_INVALID_ARG;
     if (max_tokens <= c->cap_tokens) return MM_OK;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
-    const int64_t npairs = max_tokens * c->k;
+    const int kk = mm::slots(c), P = mm::pw(c);              // slots per token, physical experts
+    const int64_t npairs = max_tokens * kk;
     // each non-empty segment adds < kSegAlign pad rows and < 1 partial token tile
-    const int64_t busy = npairs < c->P ? npairs : c->P;
+    const int64_t busy = npairs < P ? npairs : P;
     const int64_t rows = npairs + busy * (mm::kSegAlign - 1) + mm::kSegAlign;
     // token tiles: kTokTile rows on the large-input path, kSmallTile rows in the fused kernel
-    const int64_t small_pairs = npairs < int64_t(mm::kSmallMaxTokens) * c->k ? npairs : int64_t(mm::kSmallMaxTokens) * c->k;
+    const int64_t small_pairs = npairs < int64_t(mm::kSmallMaxTokens) * kk ? npairs : int64_t(mm::kSmallMaxTokens) * kk;
     const int64_t tiles = std::max(npairs / mm::kTokTile, small_pairs / mm::kSmallTile) + busy + 1;
     const int64_t chunks = (npairs + mm::kChunkPairs - 1) / mm::kChunkPairs;
     const int64_t H = c->H, I = c->I;
@@ -398,9 +421,9 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     size_t bytes = 0;
     auto add = [&](size_t n) { bytes += (n + 255) & ~size_t(255); };
     add(npairs * 4 * 4);                      // idx, phys, pos, wgt
-    add(chunks * c->P * 4);
-    add((c->P + 1) * 4);
-    add(c->P * 4);                            // first tile of each expert
+    add(chunks * P * 4);
+    add((P + 1) * 4);
+    add(P * 4);                               // first tile of each expert
     add(tiles * 4 * 4 + 8);                   // tile table, done1, num_tiles, unit counter
     const int64_t eb = c->act == MM_ACT_BF16 ? 2 : 1;     // bytes per dispatched activation element
     add(rows * H * eb);
@@ -424,9 +447,9 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     c->phys = carve<int32_t>(p, npairs);
     c->pos = carve<int32_t>(p, npairs);
     c->wgt = carve<float>(p, npairs);
-    c->chunk_hist = carve<int32_t>(p, chunks * c->P);
-    c->off = carve<int32_t>(p, c->P + 1);
-    c->toff = carve<int32_t>(p, c->P);
+    c->chunk_hist = carve<int32_t>(p, chunks * P);
+    c->off = carve<int32_t>(p, P + 1);
+    c->toff = carve<int32_t>(p, P);
     c->tile_expert = carve<int32_t>(p, tiles);
     c->tile_row0 = carve<int32_t>(p, tiles);
     c->tile_rows = carve<int32_t>(p, tiles);
@@ -589,13 +612,13 @@ static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* 
     }
     int32_t rows = 0;
     CK(cudaDeviceSynchronize());
-    CK(cudaMemcpy(&rows, c->off + c->P, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&rows, c->off + mm::pw(c), sizeof(int32_t), cudaMemcpyDeviceToHost));
     *rows_out = rows;
-    const size_t pairs = static_cast<size_t>(c->last_T) * c->k;
+    const size_t pairs = static_cast<size_t>(c->last_T) * mm::slots(c);
     const bool a16 = c->ws_act == MM_ACT_BF16;
     switch (stage) {
         case 0: case 1: case 2: case 3: *bytes = pairs * 4; break;
-        case 4: *bytes = (c->P + 1) * 4; break;
+        case 4: *bytes = (mm::pw(c) + 1) * 4; break;
         case 5: *bytes = static_cast<size_t>(rows) * c->H * (a16 ? 2 : 1); break;
         case 6: *bytes = a16 ? 0 : static_cast<size_t>(rows) * c->H / 32; break;
         case 7: *bytes = static_cast<size_t>(rows) * c->I * (a16 ? 2 : 1); break;

@@ -57,7 +57,7 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.status = c->status;
     g.H = c->H;
     g.I = c->I;
-    g.P = c->P;
+    g.P = pw(c);
     g.phases = 3;
     g.fault = c->fault;
 }

@@ -169,6 +169,7 @@ struct GemmArgs {
 struct mm_ctx {
     int dev = 0, sms = 0;
     int E = 0, P = 0, k = 0, H = 0, I = 0;
+    int ns = 0;                     // fused shared experts (mm_set_shared_experts): physical P .. P+ns-1
     int small_max = 512, large_min = 1024;
     int route = MM_ROUTE_AUTO, layer = 0, recording = 0;
     int fault = 0;                  // mm::FaultSite
@@ -234,6 +235,11 @@ enum FaultSite {
 };
 
 // host-side launchers (return cudaGetLastError of the launch)
+// slots per token (k routed + the shared experts) and physical experts with
+// weights (P routed + the shared experts)
+inline int slots(const mm_ctx* c) { return c->k + c->ns; }
+inline int pw(const mm_ctx* c) { return c->P + c->ns; }
+
 cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias, int64_t T, cudaStream_t s);
 cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s);
 cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);

@@ -277,19 +277,21 @@ cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias
     a.E = c->E;
     a.k = c->k;
     a.R = c->R;
+    a.ns = c->ns;
+    a.P = c->P;
     route_kernel<<<grid_for(T, kRouteWarps), kRouteWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
 {
-    const int64_t npairs = T * c->k;
+    const int64_t npairs = T * slots(c);
     const int nchunks = static_cast<int>((npairs + kChunkPairs - 1) / kChunkPairs);
-    hist_kernel<<<nchunks, 256, 0, s>>>(c->phys, npairs, c->P, c->chunk_hist);
+    hist_kernel<<<nchunks, 256, 0, s>>>(c->phys, npairs, pw(c), c->chunk_hist);
     ScanArgs a;
     a.chunk_hist = c->chunk_hist;
     a.nchunks = nchunks;
-    a.P = c->P;
+    a.P = pw(c);
     a.off = c->off;
     a.toff = c->toff;
     a.tile_expert = c->tile_expert;
@@ -298,7 +300,7 @@ cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
     a.num_tiles = c->num_tiles;
     a.done1 = c->done1;
     scan_kernel<<<1, 512, 0, s>>>(a);
-    scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(c->phys, npairs, c->P, c->chunk_hist, c->off, c->pos);
+    scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(c->phys, npairs, pw(c), c->chunk_hist, c->off, c->pos);
     return cudaGetLastError();
 }
 
@@ -306,7 +308,7 @@ cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T
 {
     const int64_t threads = T * (c->H / 32);
     quant_dispatch_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hidden), T, c->H,
-                                                                 c->k, c->pos, c->phys, c->off, c->toff, c->xq,
+                                                                 slots(c), c->pos, c->phys, c->off, c->toff, c->xq,
                                                                  c->xs_t);
     return cudaGetLastError();
 }
@@ -314,7 +316,7 @@ cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T
 cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s)
 {
     const int64_t threads = T * (c->H / 8);
-    dispatch16_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const uint4*>(hidden), T, c->H, c->k,
+    dispatch16_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const uint4*>(hidden), T, c->H, slots(c),
                                                              c->pos, reinterpret_cast<uint4*>(c->xq));
     return cudaGetLastError();
 }
@@ -322,7 +324,7 @@ cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cu
 cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s)
 {
     const int64_t threads = T * (c->H / 8);
-    combine_kernel<<<grid_for(threads, 256), 256, 0, s>>>(c->y, c->wgt, c->pos, T, c->H, c->k,
+    combine_kernel<<<grid_for(threads, 256), 256, 0, s>>>(c->y, c->wgt, c->pos, T, c->H, slots(c),
                                                           static_cast<__nv_bfloat16*>(out));
     return cudaGetLastError();
 }

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = a.route.T;
-    const int k = a.route.k, P = a.P, H = g.H;
+    const int k = a.route.k + a.route.ns, P = a.P, H = g.H;     // slots per token, physical experts
     const int N = static_cast<int>(T) * k;
     uint64_t* stamp = a.stamps + static_cast<int64_t>(blockIdx.x) * 8;
     if (threadIdx.x == 0) stamp[0] = globaltimer();
@@ -366,6 +366,8 @@ cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logit
     a.route.T = T;
     a.route.E = c->E;
     a.route.k = c->k;
+    a.route.ns = c->ns;
+    a.route.P = c->P;
     a.route.R = c->R;
     a.x = static_cast<const __nv_bfloat16*>(hidden);
     a.out = static_cast<__nv_bfloat16*>(out);
@@ -379,7 +381,7 @@ cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logit
     a.xs_t = c->xs_t;
     a.bar = c->grid_bar;
     a.stamps = c->stamps;
-    a.P = c->P;
+    a.P = pw(c);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c->sms));
     cfg.blockDim = dim3(kThreads);

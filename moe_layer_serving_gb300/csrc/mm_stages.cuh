@@ -56,12 +56,13 @@ struct RouteArgs {
     const float* bias;     // [E] or null
     const int32_t* map;    // [E, R]
     const int32_t* rc;     // [E]
-    int32_t* idx;          // [T, k]
-    float* w;              // [T, k]
-    int32_t* phys;         // [T, k]
+    int32_t* idx;          // [T, k + ns]
+    float* w;              // [T, k + ns]
+    int32_t* phys;         // [T, k + ns]
     int64_t* counts;       // [E] of the bound layer, or null when not recording
     int64_t T;
     int E, k, R;
+    int ns, P;             // fused shared experts: slot k + s -> physical P + s, weight 1
 };
 
 // Order-preserving map of a binary32 key to uint32 (larger key, larger code).
@@ -78,7 +79,9 @@ __device__ __forceinline__ uint32_t key_code(float f)
 // those keys and, among the lanes that hold it, the lowest expert index (ties
 // go to the lower expert), so k rounds select the experts in order.  Lane j
 // keeps the j-th selection; lanes 0..k-1 write idx/w/phys and count the
-// selections into shared memory (hist != null) or the global table.
+// selections into shared memory (hist != null) or the global table; lanes
+// k..k+ns-1 write the token's fused shared-expert slots (logical id E + s,
+// weight 1, physical P + s), which are never counted.
 template <int VPL>
 __device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int lane, int* hist)
 {
@@ -134,16 +137,22 @@ __device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int l
     // sum of the selected scores in selection order (the same in every lane)
     float S = __shfl_sync(0xFFFFFFFFu, my_s, 0);
     for (int j = 1; j < a.k; ++j) S = __fadd_rn(S, __shfl_sync(0xFFFFFFFFu, my_s, j));
+    const int kk = a.k + a.ns;
     if (lane < a.k) {
         const int e = my_e;
         const uint32_t slot = static_cast<uint32_t>(t + lane) % static_cast<uint32_t>(a.rc[e]);
-        a.idx[t * a.k + lane] = e;
-        a.w[t * a.k + lane] = __fdiv_rn(my_s, S);
-        a.phys[t * a.k + lane] = a.map[e * a.R + static_cast<int>(slot)];
+        a.idx[t * kk + lane] = e;
+        a.w[t * kk + lane] = __fdiv_rn(my_s, S);
+        a.phys[t * kk + lane] = a.map[e * a.R + static_cast<int>(slot)];
         if (a.counts) {
             if (hist) atomicAdd(&hist[e], 1);
             else atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + e), 1ull);
         }
+    } else if (lane < kk) {
+        const int sh = lane - a.k;
+        a.idx[t * kk + lane] = a.E + sh;
+        a.w[t * kk + lane] = 1.0f;
+        a.phys[t * kk + lane] = a.P + sh;
     }
 }
 

@@ -23,15 +23,17 @@ def weights(cfg, physical=True):
 class Run:
     """One handle with weights uploaded; forward() runs and collects dumps."""
 
-    def __init__(self, cfg, W=None, eplb=True, cap=None, act=0):
+    def __init__(self, cfg, W=None, eplb=True, cap=None, act=0, shared=0):
         import torch
         import moe_layer_serving_gb300 as mm
         self.torch, self.mm, self.cfg = torch, mm, cfg
         self.dev = torch.device("cuda:0")
         self.op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I)
-        self.act = act
+        self.act, self.shared = act, shared
         if act:
             self.op.set_activation_format(act)
+        if shared:
+            self.op.set_shared_experts(shared)
         W = weights(cfg) if W is None else W
         wt = [torch.from_numpy(np.ascontiguousarray(a)).to(self.dev) for a in W]
         self.op.set_weights(*wt)
@@ -59,7 +61,7 @@ class Run:
         status = self.op.get_status()
         res = {"out": out.view(t.int16).cpu().numpy().view(np.uint16), "status": status}
         if dumps:
-            T, k = hidden.shape[0], self.cfg.k
+            T, k = hidden.shape[0], self.cfg.k + self.shared
             for stage, (name, _) in self.mm.DUMP_STAGES.items():
                 a = self.op.debug_dump(stage)
                 if stage <= 3:
@@ -118,20 +120,22 @@ def assert_mxfp8_close(q_gpu, s_gpu, q_ref, s_ref, min_equal=0.999):
     return same
 
 
-def _check_routing(cfg, res, logits, bias, map_rc):
+def _check_routing(cfg, res, logits, bias, map_rc, shared=0):
     """Routing, physical ids, segment offsets and dispatch order (all tokens, exact)."""
     k, P = cfg.k, cfg.P
     m, rc = map_rc if map_rc is not None else (None, None)
     idx, w = oracle.route(logits, bias, k)
-    assert np.array_equal(res["idx"], idx), "routing indices differ"
-    assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32)), "routing weights differ"
     if m is None:
         m_, rc_ = np.arange(cfg.E, dtype=np.int32)[:, None], np.ones(cfg.E, np.int32)
     else:
         m_, rc_ = m, rc
     phys = oracle.eplb(idx, m_, rc_)
+    if shared:
+        idx, w, phys = oracle.append_shared(idx, w, phys, cfg.E, P, shared)
+    assert np.array_equal(res["idx"], idx), "routing indices differ"
+    assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32)), "routing weights differ"
     assert np.array_equal(res["phys"], phys), "physical experts differ"
-    off_o, order, pos_o = oracle.permute(phys, P)
+    off_o, order, pos_o = oracle.permute(phys, P + shared)
     cnt = np.diff(off_o)
     padded = (cnt + 15) // 16 * 16
     off_g = np.concatenate([[0], np.cumsum(padded)])
@@ -168,7 +172,7 @@ def assert_out_close_a16(got_bits, ref_bits, what="", mag=None):
     return rel
 
 
-def check_against_oracle_a16(cfg, res, hidden, logits, bias, W, map_rc, token_sel=None):
+def check_against_oracle_a16(cfg, res, hidden, logits, bias, W, map_rc, token_sel=None, shared=0):
     """Every stage of one a16w4 GPU forward against the oracle's bf16 variant.
 
     Routing and dispatch exact for all tokens; for token_sel: the dispatched
@@ -176,13 +180,13 @@ def check_against_oracle_a16(cfg, res, hidden, logits, bias, W, map_rc, token_se
     GEMM2 + combine teacher-forced on the GPU's h within bf16 rounding, and
     the output end to end.
     """
-    T, k = hidden.shape[0], cfg.k
+    T, k = hidden.shape[0], cfg.k + shared
     m, rc = map_rc if map_rc is not None else (None, None)
-    idx, w, phys = _check_routing(cfg, res, logits, bias, map_rc)
+    idx, w, phys = _check_routing(cfg, res, logits, bias, map_rc, shared)
     sel = np.arange(T) if token_sel is None else np.asarray(token_sel)
     for j in range(k):
         assert np.array_equal(res["xd"][res["pos"][sel, j]], hidden[sel]), "dispatched rows differ"
-    ref = oracle.forward(hidden[sel], logits[sel], bias, k, W, m, rc, token_ids=sel, act="bf16")
+    ref = oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel, act="bf16", shared=shared)
     rows = res["pos"][sel].ravel()                        # pair order (t, j)
     a, b = bf16_f64(res["hb"][rows]), bf16_f64(ref["hb"])
     # one bf16 step of the element, plus an absolute 2^-14 rms(h) for elements
@@ -210,22 +214,26 @@ def check_against_oracle_a16(cfg, res, hidden, logits, bias, W, map_rc, token_se
     return rel, ref
 
 
-def check_against_oracle(cfg, res, hidden, logits, bias, W, map_rc, token_sel=None, check_hq=True):
+def check_against_oracle(cfg, res, hidden, logits, bias, W, map_rc, token_sel=None, check_hq=True, shared=0):
     """Every stage of one GPU forward against the oracle.
 
     Routing, physical ids and the dispatch order are checked for all tokens;
     the expert FFN and the output for token_sel (all tokens when None).
+    ``shared``: fused shared experts (the last ``shared`` experts of W).
     """
     T, k, P = hidden.shape[0], cfg.k, cfg.P
     m, rc = map_rc if map_rc is not None else (None, None)
     idx, w = oracle.route(logits, bias, k)
-    assert np.array_equal(res["idx"], idx), "routing indices differ"
-    assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32)), "routing weights differ"
     if m is None:
         m_, rc_ = np.arange(cfg.E, dtype=np.int32)[:, None], np.ones(cfg.E, np.int32)
     else:
         m_, rc_ = m, rc
     phys = oracle.eplb(idx, m_, rc_)
+    if shared:
+        idx, w, phys = oracle.append_shared(idx, w, phys, cfg.E, P, shared)
+    k, P = k + shared, P + shared                           # slots per token, physical experts
+    assert np.array_equal(res["idx"], idx), "routing indices differ"
+    assert np.array_equal(res["weights"].view(np.uint32), w.view(np.uint32)), "routing weights differ"
     assert np.array_equal(res["phys"], phys), "physical experts differ"
     off_o, order, pos_o = oracle.permute(phys, P)
     cnt = np.diff(off_o)
@@ -244,7 +252,7 @@ def check_against_oracle(cfg, res, hidden, logits, bias, W, map_rc, token_sel=No
         assert np.array_equal(res["xq"][rows], xq), "activation codes differ"
         assert np.array_equal(res["xs"][rows], xs), "activation scales differ"
 
-    ref = oracle.forward(hidden[sel], logits[sel], bias, k, W, m, rc, token_ids=sel)
+    ref = oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel, shared=shared)
     assert np.array_equal(ref["idx"], idx[sel])
     rows = res["pos"][sel].ravel()                        # pair order (t, j)
     if check_hq:

@@ -163,3 +163,18 @@ def test_graph_capture_replay_matches_eager(torch):
     assert run.op.get_status() == 0
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     run.close()
+
+
+@pytest.mark.parametrize("T", [40, 1100])
+def test_fused_shared_expert(torch, T):
+    import moe_layer_serving_gb300 as mm
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T)
+    wide = dataclasses.replace(cfg, E=cfg.E + 1, P=cfg.P + 1)
+    W = synthetic.make_all_weights(wide)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    run = gpu_util.Run(cfg, W, cap=T, act=mm.ACT_BF16, shared=1)
+    res = run.forward(hidden, logits, bias)
+    run.close()
+    assert res["status"] == 0
+    assert np.all(res["idx"][:, cfg.k] == cfg.E) and np.all(res["weights"][:, cfg.k] == 1.0)
+    gpu_util.check_against_oracle_a16(cfg, res, hidden, logits, bias, W, None, shared=1)

@@ -171,3 +171,65 @@ def test_special_values_and_routing_ties(route):
     rest = np.array([t for t in range(cfg.T) if t != 2])
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, rest)
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, np.array([2]))
+
+
+def _shared_weights(cfg, shared, physical_map=False):
+    # routed physical experts' weights, then `shared` further experts' weights
+    import dataclasses
+    wide = dataclasses.replace(cfg, E=cfg.E + shared, P=cfg.E + shared)
+    Wl = synthetic.make_all_weights(wide, physical=False)
+    if physical_map:
+        p2l = synthetic.physical_to_logical(cfg)
+        routed = [a[p2l] for a in Wl]
+    else:
+        routed = [a[:cfg.E] for a in Wl]
+    return tuple(np.concatenate([r, a[cfg.E:]]) for r, a in zip(routed, Wl))
+
+
+@pytest.mark.parametrize("T,route,shared", [(40, 1, 1), (40, 2, 1), (300, 1, 2), (1100, 2, 1)])
+def test_fused_shared_experts(T, route, shared):
+    # every token also goes to the shared experts (weight 1) on both paths
+    import dataclasses
+    import moe_layer_serving_gb300 as mm
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T)
+    W = _shared_weights(cfg, shared)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    run = gpu_util.Run(cfg, W, cap=T, shared=shared)
+    run.op.set_route(mm.ROUTE_SMALL if route == 1 else mm.ROUTE_LARGE)
+    res = run.forward(hidden, logits, bias)
+    info = run.op.last_info()
+    run.close()
+    assert res["status"] == 0 and info[0] == route
+    assert np.all(res["idx"][:, cfg.k:] == cfg.E + np.arange(shared))
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, shared=shared)
+
+
+def test_fused_shared_expert_with_replicas_and_recording():
+    # P > E (two redundant replicas) with the recorder on: the counts hold the
+    # routed selections only
+    import dataclasses
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=200, P=10, recording=True)
+    W = _shared_weights(cfg, 1, physical_map=True)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    run = gpu_util.Run(cfg, W, cap=cfg.T, shared=1)
+    run.op.set_recording(True)
+    res = run.forward(hidden, logits, bias)
+    counts = run.op.read_counts(0)
+    run_map = run.map
+    run.close()
+    assert res["status"] == 0
+    idx, _ = oracle.route(logits, bias, cfg.k)
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=cfg.E))
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, run_map, shared=1)
+
+
+def test_fused_shared_expert_decode_shapes():
+    # the decode layer (H = 7168, I = 2048, 256 experts, top-6) plus one shared expert
+    cfg = synthetic.CONFIGS[1]
+    W = _shared_weights(cfg, 1)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    run = gpu_util.Run(cfg, W, cap=cfg.T, shared=1)
+    res = run.forward(hidden, logits, bias)
+    run.close()
+    assert res["status"] == 0
+    gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(cfg.T, 16), shared=1)
