@@ -62,6 +62,8 @@ def test_null_handle_calls_are_invalid(built):
     assert L.mm_forward(None, None, None, None, None, 1, None) == mm.MM_ERR_INVALID_ARG
     assert L.mm_bind_layer(None, 0) == mm.MM_ERR_INVALID_ARG
     assert L.mm_reserve(None, 16) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_set_shared_experts(None, 1) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_set_activation_format(None, 0) == mm.MM_ERR_INVALID_ARG
     assert L.mm_destroy(None) == mm.MM_OK
     assert L.mm_status_string(4) == b"token count above capacity"
 

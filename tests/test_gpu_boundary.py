@@ -268,3 +268,22 @@ def test_tile_table_and_tile_size_choice(torch, case):
         assert np.bincount(res["phys"].ravel(), minlength=cfg.P)[0] > 64
     _check_tiles(res, cfg.P, 64 if case == "short" else 128)
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(T, 32))
+
+
+def test_shared_expert_limits_and_weight_reset(torch):
+    # k + S <= MM_MAX_TOPK and P + S <= MM_MAX_EXPERTS; changing S drops the
+    # weights (forward is not ready until they are set again)
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I)
+    L = mm.lib()
+    assert L.mm_set_shared_experts(op.handle, -1) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_set_shared_experts(op.handle, 8 - cfg.k + 1) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_set_shared_experts(op.handle, 8 - cfg.k) == mm.MM_OK
+    op.set_shared_experts(1)
+    op.reserve(cfg.T)
+    x = torch.zeros(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(cfg.T, cfg.E, device="cuda")
+    assert L.mm_forward(op.handle, x.data_ptr(), lg.data_ptr(), None, x.data_ptr(), cfg.T, None) == \
+        mm.MM_ERR_NOT_READY
+    op.close()
