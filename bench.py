@@ -117,6 +117,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline leg")
     ap.add_argument("--route", choices=["auto", "small", "large"], default="auto",
                     help="path: auto (fused kernel up to 512 tokens), or force the fused or the multi-launch path")
+    ap.add_argument("--shared", type=int, default=0,
+                    help="fused shared experts: slots per token beyond top-k, weight 1 (mm_set_shared_experts)")
     ap.add_argument("--act", choices=["mxfp8", "bf16"], default="mxfp8",
                     help="activation format: mxfp8 (a8w4, the fused operator) or bf16 (the a16w4 variant)")
     ap.add_argument("--experts", type=int, default=0,
@@ -124,11 +126,11 @@ def parse():
     return ap.parse_args()
 
 
-def workload_config(cfg, act="mxfp8", route="auto"):
+def workload_config(cfg, act="mxfp8", route="auto", shared=0):
     name = "a8w4" if act == "mxfp8" else "a16w4"
-    suffix = "" if route == "auto" else f"-{route}-path"
+    suffix = ("" if route == "auto" else f"-{route}-path") + (f"-shared{shared}" if shared else "")
     return {"workload": f"moe-layer-{name}-T{cfg.T}{suffix}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-            "P": cfg.P, "topk": cfg.k, "routing": "zipf" if cfg.zipf_s else "uniform",
+            "P": cfg.P, "topk": cfg.k, "shared_experts": shared, "routing": "zipf" if cfg.zipf_s else "uniform",
             "eplb_redundant": cfg.P - cfg.E, "l2": "weights 6 GB > L2, no flush",
             "parallelism": "replicas"}
 
@@ -183,28 +185,37 @@ class ClockSampler:
 SOAK_S = 1.0
 
 
-def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens, act="mxfp8"):
+def oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n_tokens, act="mxfp8", shared=0):
     """Tokens/s of the CPU oracle on the first n_tokens of the batch."""
     import oracle
     sel = np.arange(min(n_tokens, hidden.shape[0]))
     m, rc = pmap if pmap else (None, None)
     t0 = time.perf_counter()
-    oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel, act=act)
+    oracle.forward(hidden[sel], logits[sel], bias, cfg.k, W, m, rc, token_ids=sel, act=act, shared=shared)
     dt = time.perf_counter() - t0
     return sel.size / dt, dt, sel.size
 
 
-def oracle_bounded_rate(cfg, hidden, logits, bias, W, pmap, seconds, act="mxfp8"):
+def with_shared_weights(cfg, W, shared):
+    """W (the P routed physical experts) followed by `shared` further experts,
+    drawn as logical experts E .. E+shared-1 of the same seeded generator."""
+    if not shared:
+        return W
+    extra = [synthetic.make_expert_weights(cfg, cfg.E + s) for s in range(shared)]
+    return tuple(np.concatenate([a, np.stack([x[i] for x in extra])]) for i, a in enumerate(W))
+
+
+def oracle_bounded_rate(cfg, hidden, logits, bias, W, pmap, seconds, act="mxfp8", shared=0):
     """Tokens/s of the CPU oracle over about `seconds` of work: the token sample
     doubles from 8 until one run takes a quarter of that or covers the batch,
     then that sample runs until the time is spent (at most 8 runs)."""
     n = min(8, cfg.T)
-    rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, act)
+    rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, act, shared)
     while dt < seconds / 4 and n < cfg.T:
-        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, min(2 * n, cfg.T), act)
+        rate, dt, n = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, min(2 * n, cfg.T), act, shared)
     toks, total, reps = n, dt, 1
     while total < seconds and reps < 8:
-        _, d, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, act)
+        _, d, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, act, shared)
         toks, total, reps = toks + n, total + d, reps + 1
     return toks / total, total, n, reps
 
@@ -240,14 +251,14 @@ def run_reference(args):
     import oracle
     cfg = synthetic.CONFIGS[args.config]
     hidden, logits, bias = synthetic.make_activations(cfg)
-    W = synthetic.make_all_weights(cfg)
+    W = with_shared_weights(cfg, synthetic.make_all_weights(cfg), args.shared)
     pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
     n = min(args.cpu_sample, cfg.T)
     for _ in range(max(0, args.warmup and 1)):
-        oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, 1, args.act)
+        oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, 1, args.act, args.shared)
     times = []
     for _ in range(args.steps):
-        _, dt, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, args.act)
+        _, dt, _ = oracle_sample_rate(cfg, hidden, logits, bias, W, pmap, n, args.act, args.shared)
         times.append(dt)
     per_tok = statistics.median(times) / n
     value = 1.0 / per_tok
@@ -255,7 +266,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * cfg.T * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(cfg, args.act),
+        "data": "synthetic", "config": workload_config(cfg, args.act, shared=args.shared),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": f"first {n} of {cfg.T} tokens per step, all stages"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -285,10 +296,12 @@ def main():
         import dataclasses
         cfg = dataclasses.replace(cfg, E=args.experts, P=args.experts, zipf_s=0.0)
     hidden, logits, bias = synthetic.make_activations(cfg)
-    W = synthetic.make_all_weights(cfg)
+    W = with_shared_weights(cfg, synthetic.make_all_weights(cfg), args.shared)
     pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
 
     op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I)
+    if args.shared:
+        op.set_shared_experts(args.shared)
     wt = [torch.from_numpy(a).to(dev) for a in W]
     op.set_weights(*wt)
     del wt
@@ -382,7 +395,7 @@ def main():
     if os.path.exists(pk):
         peaks = json.load(open(pk))
     kname = "gemm16_kernel" if a16 else ("small_kernel" if route == 1 else "gemm_kernel")
-    wname = workload_config(cfg, args.act, args.route)["workload"]
+    wname = workload_config(cfg, args.act, args.route, args.shared)["workload"]
     if cfg.T <= 512:
         alg = touched * expert_bytes(cfg)           # weight streaming: the touched experts' bytes
         achieved = alg / (kern_ms / 1e3) / 1e9
@@ -391,7 +404,7 @@ def main():
                 "traffic": measured_traffic(kname, wname), "kernel": kname, "algorithmic_bytes": alg,
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
     else:
-        flops = 6.0 * cfg.T * cfg.k * cfg.H * cfg.I
+        flops = 6.0 * cfg.T * (cfg.k + args.shared) * cfg.H * cfg.I
         achieved = flops / (kern_ms / 1e3) / 1e12
         # bf16 MMAs (a16w4) against the measured bf16 rate; fp8-class MMAs at 2x it
         mult = 1.0 if a16 else 2.0
@@ -405,14 +418,15 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16xe2m1->f32" if a16 else "e4m3xe2m1->f32",
-        "data": "synthetic (seeded, random-init weights)", "config": workload_config(cfg, args.act, args.route), "clocks": clk, "gpu_launches": launches * args.steps,
+        "data": "synthetic (seeded, random-init weights)", "config": workload_config(cfg, args.act, args.route, args.shared), "clocks": clk, "gpu_launches": launches * args.steps,
         "route": "small" if route == 1 else "large", "kernel_ms": kern_ms, "touched_experts": touched,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": roof,
     }
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
-        rate, total, n, reps = oracle_bounded_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_seconds, args.act)
+        rate, total, n, reps = oracle_bounded_rate(cfg, hidden, logits, bias, W, pmap, args.cpu_seconds, args.act,
+                                                   args.shared)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
                                 "sample": f"{reps} x first {n} of {cfg.T} tokens, all stages, {total:.1f} s timed"}
     if rank == 0:

@@ -86,7 +86,7 @@ def test_clock_window_keeps_only_samples_inside_it():
 def test_bounded_oracle_sample_grows_then_repeats(monkeypatch):
     calls = []
 
-    def fake(cfg, hidden, logits, bias, W, pmap, n, act="mxfp8"):
+    def fake(cfg, hidden, logits, bias, W, pmap, n, act="mxfp8", shared=0):
         n = min(n, cfg.T)
         calls.append(n)
         dt = 0.1 * n                    # 0.1 s per token
