@@ -3,10 +3,12 @@
 
 One step = one layer forward (routing, EPLB remap/record, MXFP8 quant,
 dispatch, GEMM1+SwiGLU+requant, GEMM2, combine) over one batch of seeded
-synthetic tokens.  Default workload: the decode (small-input) layer, T=64
-tokens, H=7168, I=2048, 256 experts, top-6.  The expert weights (6 GB of
-MXFP4) are larger than L2, so consecutive steps stream them from HBM; no
-flush is needed.
+synthetic tokens.  Default workload: the largest one-GPU layer, T=16384
+tokens, H=7168, I=2048, 256 logical experts on 320 physical (64 redundant
+replicas), top-6, Zipf-skewed routing with load recording (the large-input
+path); --config 1 is the decode (small-input) layer, T=64.  The expert
+weights (6-7.5 GB of MXFP4) and the dispatched rows are larger than L2, so
+consecutive steps stream them from HBM; no flush is needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
@@ -107,7 +109,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=64,
                     help="tokens per step in the reference arm's sample (the oracle dequantises each touched "
@@ -123,16 +125,38 @@ def parse():
                     help="activation format: mxfp8 (a8w4, the fused operator) or bf16 (the a16w4 variant)")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E = P (a smaller case of the same kernels, for profiler captures)")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="divide T, E and P by this factor, keeping the routing shape, the rows per expert and "
+                         "the redundant-replica share (a smaller case for profiler captures)")
     return ap.parse_args()
+
+
+def scaled_down(cfg, f: int):
+    """The same workload with T, E and P divided by f: equal rows per expert
+    (T k / E), the same routing recipe and the same share of redundant
+    replicas, so its kernels do 1/f of the work of the full one."""
+    import dataclasses
+    if cfg.T % f or cfg.E % f or cfg.P % f or cfg.E // f < cfg.k:
+        raise SystemExit(f"--scale-down {f} does not divide config {cfg.cid}")
+    return dataclasses.replace(cfg, T=cfg.T // f, E=cfg.E // f, P=cfg.P // f)
+
+
+def routing_label(cfg) -> str:
+    if cfg.zipf_s:
+        return f"zipf s={cfg.zipf_s:g} logit offset + N(0,1)"
+    return "N(0,1) logits" + (f" + N(0,{cfg.bias_std:g}) selection bias" if cfg.bias_std else "")
 
 
 def workload_config(cfg, act="mxfp8", route="auto", shared=0):
     name = "a8w4" if act == "mxfp8" else "a16w4"
     suffix = ("" if route == "auto" else f"-{route}-path") + (f"-shared{shared}" if shared else "")
+    full = synthetic.CONFIGS.get(cfg.cid)
+    if full is not None and (cfg.E, cfg.P) != (full.E, full.P):
+        suffix += f"-E{cfg.E}-P{cfg.P}"          # a reduced case of the workload (profiler captures)
     return {"workload": f"moe-layer-{name}-T{cfg.T}{suffix}", "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-            "P": cfg.P, "topk": cfg.k, "shared_experts": shared, "routing": "zipf" if cfg.zipf_s else "uniform",
-            "eplb_redundant": cfg.P - cfg.E, "l2": "weights 6 GB > L2, no flush",
-            "parallelism": "replicas"}
+            "P": cfg.P, "topk": cfg.k, "shared_experts": shared, "routing": routing_label(cfg),
+            "eplb_redundant": cfg.P - cfg.E, "recording": bool(cfg.recording),
+            "l2": "weights and dispatched rows > L2, no flush", "parallelism": "replicas"}
 
 
 class ClockSampler:
@@ -295,6 +319,8 @@ def main():
     if args.experts:
         import dataclasses
         cfg = dataclasses.replace(cfg, E=args.experts, P=args.experts, zipf_s=0.0)
+    if args.scale_down > 1:
+        cfg = scaled_down(cfg, args.scale_down)
     hidden, logits, bias = synthetic.make_activations(cfg)
     W = with_shared_weights(cfg, synthetic.make_all_weights(cfg), args.shared)
     pmap = synthetic.make_eplb_map(cfg)[:2] if cfg.P != cfg.E else None
@@ -411,6 +437,7 @@ def main():
         peak = peaks.get("bf16_tflops", 1900.0) * mult
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": measured_traffic(kname, wname), "kernel": kname, "algorithmic_flops": flops,
+                "step_frac": flops / (ms / 1e3) / 1e12 / peak,
                 "peak_source": ("measured bf16" if a16 else "measured bf16 x 2") if "bf16_tflops" in peaks
                 else ("fallback" if a16 else "fallback x 2")}
 

@@ -189,7 +189,10 @@ MM_API mm_status mm_reset_counts(mm_handle h, int layer);
  * (0 = none, else an mm_status value) and clear it.  After a device error it
  * also resets the fused kernel's grid-barrier count (an aborted launch may
  * have left arrivals missing), so call it before the next forward once a
- * forward has failed on the device. */
+ * forward has failed on the device.  Until it is called, a forward that takes
+ * the fused small-input kernel does no work at all (its output is not
+ * written) and the error stays latched, so a forward made after an unread
+ * failure never passes off stale output as a success. */
 MM_API mm_status mm_get_status(mm_handle h, int *device_code);
 
 /* Intermediates of the last forward, for tests.  Synchronous.  `stage`:
@@ -271,8 +274,9 @@ MM_API mm_status mm_profile_end(mm_handle h, float *ms_out, int max_out, int *n_
  *
  * Scratch lives in a 256 KB array inside the library, not in allocated
  * memory; every GPU that loads the library holds it until the process exits.
- * The first call on a device looks up that array's device address (make it
- * before any stream capture).  All calls share the array, so calls whose
+ * The first call on a device, and the first call after that device's context
+ * was created anew (cudaDeviceReset), looks up that array's device address:
+ * make it before any stream capture.  All calls share the array, so calls whose
  * kernels overlap on the GPU (different streams, or different threads without
  * ordering) race and must not be made; calls in one stream are fine.
  * Asynchronous on `stream`; allocates nothing. */

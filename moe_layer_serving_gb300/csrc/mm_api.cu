@@ -215,13 +215,29 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
     const size_t b1 = mm::w_blocks(o1, static_cast<int>(P)), b2 = mm::w_blocks(o2, static_cast<int>(P));
     const size_t n_w1 = b1 * 8192, n_w1s = b1 * 512;
     const size_t n_w2 = b2 * 8192, n_w2s = b2 * 512;
-    if (!c->w1) {
-        if (cudaMalloc(&c->w1, n_w1) != cudaSuccess || cudaMalloc(&c->w1_sf, n_w1s) != cudaSuccess ||
-            cudaMalloc(&c->w2, n_w2) != cudaSuccess || cudaMalloc(&c->w2_sf, n_w2s) != cudaSuccess) {
+    if (!c->w1 || !c->w1_sf || !c->w2 || !c->w2_sf) {
+        // all four buffers or none: a failed allocation frees the others, so a
+        // later call never finds a partial set and writes through a null one
+        uint8_t* buf[4] = {c->w1, c->w1_sf, c->w2, c->w2_sf};
+        const size_t n[4] = {n_w1, n_w1s, n_w2, n_w2s};
+        bool ok = true;
+        for (int i = 0; i < 4 && ok; ++i)
+            if (!buf[i]) ok = cudaMalloc(&buf[i], n[i]) == cudaSuccess;
+        if (!ok) {
             cudaGetLastError();
+            for (uint8_t* b : buf)
+                if (b) cudaFree(b);
+            c->w1 = c->w1_sf = c->w2 = c->w2_sf = nullptr;
+            c->weights_set = false;
+            c->maps_weights = false;
             return MM_ERR_CUDA;
         }
+        c->w1 = buf[0];
+        c->w1_sf = buf[1];
+        c->w2 = buf[2];
+        c->w2_sf = buf[3];
     }
+    c->weights_set = false;     // until the re-layout below has completed
     if (n_w2 != P * H * I / 2) CK(cudaMemset(c->w2, 0, n_w2));       // absent halves of a ragged last group
     CK(mm::launch_tile_weights(w1, c->w1, static_cast<int64_t>(P * 2 * I), c->H, o1, nullptr));
     CK(mm::launch_tile_weights(w2, c->w2, static_cast<int64_t>(P * H), c->I, o2, nullptr));

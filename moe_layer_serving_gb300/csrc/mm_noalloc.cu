@@ -10,6 +10,7 @@
 // It is a single-CTA variant of the permute kernels (chunk histograms ->
 // per-expert scan into aligned segments -> stable scatter), producing
 // the same dispatch rows and segment offsets as mm_forward's permute.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -92,10 +93,47 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     }
 }
 
-// Device address of g_plan_scratch, looked up once per device.
+// Device address of g_plan_scratch, looked up once per device and context:
+// the address belongs to the module loaded into the device's current
+// context, so when that context is created anew (after cudaDeviceReset, or
+// once the primary context was released and retained again) the address is
+// looked up again.  Contexts are told apart by the driver's context id, which
+// is unique for the life of the process (a re-created context may reuse the
+// old handle's value, never its id).
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mutex;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+void* driver_fn(const char* name)
+{
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return p;
+}
+
+// id of the context current on this thread; 0 when none is bound yet
+bool current_ctx_id(unsigned long long* id)
+{
+    static CtxGetCurrentFn get_ctx = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+    static CtxGetIdFn get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId"));
+    *id = 0;
+    if (!get_ctx || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return false;
+    return !ctx || get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -113,15 +151,22 @@ extern "C" mm_status mm_plan_dispatch_static(const int32_t* phys, int64_t npairs
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_scratch_mutex);
-        if (!g_scratch_addr[dev]) {
+        unsigned long long id = 0;
+        if (!current_ctx_id(&id)) return MM_ERR_CUDA;
+        ScratchAddr& slot = g_scratch_addr[dev];
+        if (!slot.addr || id == 0 || slot.ctx_id != id) {
+            // set-up: the address of the array in the current context (this
+            // also binds the device's primary context when none is yet)
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || !p) {
                 cudaGetLastError();
                 return MM_ERR_CUDA;
             }
-            g_scratch_addr[dev] = p;
+            if (id == 0 && (!current_ctx_id(&id) || id == 0)) return MM_ERR_CUDA;
+            slot.ctx_id = id;
+            slot.addr = p;
         }
-        scratch = g_scratch_addr[dev];
+        scratch = slot.addr;
     }
     plan_kernel<<<1, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         phys, static_cast<int>(npairs), num_physical, static_cast<int32_t*>(scratch), pos, offsets);

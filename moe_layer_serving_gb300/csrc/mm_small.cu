@@ -149,6 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     small_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g,
                  const __grid_constant__ SmallArgs a)
 {
+    // An error latched by an earlier launch and not yet read by the host may
+    // have left the grid-barrier count short of a multiple of the grid: every
+    // CTA then returns at once, doing no work and touching no barrier, and the
+    // error stays latched for mm_get_status (which also resets the count).
+    // Every CTA sees the same value here: within this launch nothing can
+    // latch an error before a bounded wait has run out.
+    if (*reinterpret_cast<volatile int*>(g.status) != 0) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const GemmSmem s = gemm_smem(smem, smem + kStageRegion);

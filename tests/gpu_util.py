@@ -93,6 +93,24 @@ def sample_tokens(T, n=24, seed=0):
     return np.unique(np.clip(np.concatenate([fixed, rest]), 0, T - 1))
 
 
+def tile_edge_tokens(res, T):
+    """Tokens whose (token, slot) pairs sit in the first or the last row of
+    every token tile of one GPU forward (the tile table of debug stage 12):
+    checking them end to end covers every tile of every expert, however late
+    its units ran, with about two tokens per tile."""
+    pos = res["pos"]
+    k = pos.shape[1]
+    token_of_row = {int(r): t for t, r in zip(np.repeat(np.arange(T), k), pos.ravel())}
+    tiles = res["tiles"].reshape(-1, 3)
+    assert tiles.shape[0] > 0
+    sel = set()
+    for _, row0, rows in tiles:
+        assert rows >= 1
+        sel.add(token_of_row[int(row0)])
+        sel.add(token_of_row[int(row0 + rows - 1)])
+    return np.array(sorted(sel), dtype=np.int64)
+
+
 def bf16_f64(bits):
     return synthetic.f32_from_bf16_bits(bits).astype(np.float64)
 

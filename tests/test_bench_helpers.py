@@ -107,3 +107,23 @@ def test_bounded_oracle_sample_grows_then_repeats(monkeypatch):
 def test_weak_scaling_value_counts_every_rank():
     assert bench.weak_scaling_value(64, 1, 0.5) == pytest.approx(128000.0)
     assert bench.weak_scaling_value(64, 4, 0.5) == pytest.approx(512000.0)
+
+
+def test_scaled_down_workload_keeps_rows_per_expert_and_replica_share():
+    full = synthetic.CONFIGS[4]
+    small = bench.scaled_down(full, 8)
+    assert (small.T, small.E, small.P) == (2048, 32, 40)
+    assert small.T * small.k / small.E == full.T * full.k / full.E
+    assert (small.P - small.E) / small.E == (full.P - full.E) / full.E
+    assert (small.zipf_s, small.recording, small.H, small.I) == (full.zipf_s, full.recording, full.H, full.I)
+    name = bench.workload_config(small)["workload"]
+    assert name == "moe-layer-a8w4-T2048-E32-P40"
+    assert bench.workload_config(full)["workload"] == "moe-layer-a8w4-T16384"
+    with pytest.raises(SystemExit):
+        bench.scaled_down(full, 3)
+
+
+def test_routing_labels_name_the_recipe():
+    assert bench.workload_config(synthetic.CONFIGS[1])["routing"] == "N(0,1) logits + N(0,0.1) selection bias"
+    assert bench.workload_config(synthetic.CONFIGS[3])["routing"] == "N(0,1) logits"
+    assert bench.workload_config(synthetic.CONFIGS[4])["routing"].startswith("zipf s=1.4")

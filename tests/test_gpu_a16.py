@@ -30,7 +30,7 @@ def torch():
     return torch
 
 
-def _run(cfg, hidden, logits, bias, W, sample=None, recording=False):
+def _run(cfg, hidden, logits, bias, W, sample=None, recording=False, tiles=False):
     import moe_layer_serving_gb300 as mm
     run = gpu_util.Run(cfg, W, cap=hidden.shape[0], act=mm.ACT_BF16)
     run.op.set_recording(recording)
@@ -44,15 +44,18 @@ def _run(cfg, hidden, logits, bias, W, sample=None, recording=False):
     assert res["status"] == 0
     assert info[:2] == (2, 7)
     sel = None if sample is None else gpu_util.sample_tokens(hidden.shape[0], sample)
+    if tiles:
+        # the first and the last row of every token tile, end to end
+        sel = gpu_util.tile_edge_tokens(res, hidden.shape[0])
     rel, _ = gpu_util.check_against_oracle_a16(cfg, res, hidden, logits, bias, W, run_map, sel)
     return res, rel
 
 
-def _cfg(cid, T=None, sample=None):
+def _cfg(cid, T=None, sample=None, tiles=False):
     cfg = synthetic.CONFIGS[cid]
     hidden, logits, bias = synthetic.make_activations(cfg, T)
     W = gpu_util.weights(cfg)
-    return _run(cfg, hidden, logits, bias, W, sample, cfg.recording)
+    return _run(cfg, hidden, logits, bias, W, sample, cfg.recording, tiles)
 
 
 def test_tiny_all_tokens(torch):
@@ -90,12 +93,12 @@ def test_eplb_t512(torch):
 
 
 def test_prefill_t8192(torch):
-    _cfg(3, sample=16)
+    _cfg(3, tiles=True)             # every token tile of the layer
 
 
 def test_skewed_eplb_t16384(torch):
     # skewed routing with 64 redundant replicas and the recorder on
-    _cfg(4, sample=16)
+    _cfg(4, tiles=True)
 
 
 def test_format_switch_and_route_rules(torch):

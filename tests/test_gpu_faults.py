@@ -79,3 +79,32 @@ def test_injected_wait_times_out_in_the_a16w4_gemm(torch, T):
     assert res["status"] == 0
     ref = oracle.forward(*inputs, cfg.k, gpu_util.weights(cfg), act="bf16")
     gpu_util.assert_out_close_a16(res["out"], ref["out"], mag=gpu_util.pair_magnitude(ref, cfg.k))
+
+
+def test_forward_after_unread_failure_does_no_work(torch):
+    # A timed-out fused launch leaves the grid-barrier count short of a multiple
+    # of the grid.  A second forward made before mm_get_status must not run on
+    # that count (its barriers would release early and its output be wrong):
+    # it does no work, leaves its output untouched, and the error stays latched.
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    T = 64
+    os.environ["MM_FAULT"] = "grid_barrier"
+    try:
+        run = gpu_util.Run(cfg, cap=T)
+    finally:
+        del os.environ["MM_FAULT"]
+    hidden, logits, bias = synthetic.make_activations(cfg, T)
+    x, lg, b = run.to_dev(hidden, logits, bias)
+    out = torch.empty_like(x)
+    run.op.forward(x, lg, b, out)                    # times out on the device
+    torch.cuda.synchronize()
+    out.view(torch.int16).fill_(0x7F7F)
+    run.op.forward(x, lg, b, out)                    # no mm_get_status in between
+    torch.cuda.synchronize()
+    assert run.op.last_info()[0] == 1
+    assert bool((out.view(torch.int16) == 0x7F7F).all()), "a forward after an unread failure wrote output"
+    assert run.op.get_status() == mm.MM_ERR_TIMEOUT
+    assert run.op.last_info()[2] == SITE_GRID_BARRIER
+    assert run.op.get_status() == 0                  # read and cleared
+    run.close()

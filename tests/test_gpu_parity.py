@@ -5,9 +5,10 @@ segment offsets and dispatch order, MXFP8 activation codes and scales.
 GEMM1 requantised codes: >= 99.9% identical, the rest one e4m3 step apart.
 GEMM2 + combine fed with the GPU's hq: within bf16 rounding.
 Layer output: relative L2 <= 1e-2 and every |err| <= 0.05 rms(out).
-The decode batch is compared end to end on every token; the larger
-workloads compare sampled tokens end to end and all tokens for routing,
-remap, counts and dispatch.
+The decode batch is compared end to end on every token; the 512-token
+workload on sampled tokens; the 8192- and 16384-token workloads on the tokens
+of the first and the last row of every token tile (every tile of every
+expert); all workloads on all tokens for routing, remap, counts and dispatch.
 """
 import numpy as np
 import pytest
@@ -29,7 +30,7 @@ def _gpu():
     torch.cuda.set_device(0)
 
 
-def _cfg_run(cid, T=None, sample=None):
+def _cfg_run(cid, T=None, sample=None, tiles=False):
     cfg = synthetic.CONFIGS[cid]
     hidden, logits, bias = synthetic.make_activations(cfg, T)
     W = gpu_util.weights(cfg)
@@ -41,6 +42,10 @@ def _cfg_run(cid, T=None, sample=None):
         idx, _ = oracle.route(logits, bias, cfg.k)
         assert np.array_equal(run.op.read_counts(0), np.bincount(idx.ravel(), minlength=cfg.E)), "counts differ"
     sel = None if sample is None else gpu_util.sample_tokens(hidden.shape[0], sample)
+    if tiles:
+        # the first and the last row of every token tile, end to end
+        sel = gpu_util.tile_edge_tokens(res, hidden.shape[0])
+        assert sel.size >= res["tiles"].size // 3
     rel, _ = gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, run.map, sel)
     run.close()
     return rel
@@ -64,11 +69,11 @@ def test_config2_eplb_t512():
 
 
 def test_config3_prefill_t8192():
-    _cfg_run(3, sample=16)
+    _cfg_run(3, tiles=True)         # every token tile of the layer
 
 
 def test_config4_skewed_eplb_t16384():
-    _cfg_run(4, sample=16)
+    _cfg_run(4, tiles=True)
 
 
 def test_ragged_hidden_and_odd_shapes():

@@ -73,3 +73,52 @@ def test_static_plan_rejects_oversized_input(torch):
         mm.MM_ERR_CAPACITY
     assert L.mm_plan_dispatch_static(dummy.data_ptr(), 16, 513, dummy.data_ptr(), dummy.data_ptr(), None) == \
         mm.MM_ERR_INVALID_ARG
+
+
+def _expected_plan(phys, P):
+    """The plan from the oracle's permute over the ids inside [0, P): segments
+    padded to 16 rows, pairs in pair order inside a segment, -1 elsewhere."""
+    import oracle
+    valid = (phys >= 0) & (phys < P)
+    off_o, _, pos_o = oracle.permute(phys[valid].astype(np.int32), P)
+    padded = (np.diff(off_o) + 15) // 16 * 16
+    off = np.concatenate([[0], np.cumsum(padded)]).astype(np.int64)
+    pos = np.full(phys.size, -1, np.int64)
+    pv = phys[valid]
+    pos[valid] = off[pv] + (pos_o - off_o[pv])
+    return pos, off
+
+
+def test_static_plan_leaves_out_ids_outside_the_expert_range(torch):
+    rng = np.random.default_rng(3)
+    P = 40
+    phys = rng.integers(0, P, size=5000).astype(np.int32)
+    phys[::97] = P                  # one past the last expert
+    phys[5::131] = -3               # negative
+    phys[7::1009] = 1 << 20         # far outside
+    got_pos, got_off = _static_plan(torch, phys, P)
+    pos, off = _expected_plan(phys, P)
+    assert np.array_equal(got_off, off)
+    assert np.array_equal(got_pos, pos)
+    assert np.all(got_pos[(phys < 0) | (phys >= P)] == -1)
+
+
+def test_static_plan_at_its_limits_then_a_small_call(torch):
+    # 512 experts (the limit) and 131,072 pairs (the cap): 128 chunks x 512
+    # experts of counts fill the whole 256 KB scratch array.  A small call on
+    # the same stream right after must not see those leftovers.
+    rng = np.random.default_rng(4)
+    P = 512
+    # skewed ids so that some chunks hit every expert and some experts get many rows
+    big = np.minimum(rng.zipf(1.3, size=131072) - 1, P - 1).astype(np.int32)
+    big[:P] = np.arange(P, dtype=np.int32)
+    got_pos, got_off = _static_plan(torch, big, P)
+    pos, off = _expected_plan(big, P)
+    assert np.array_equal(got_off, off)
+    assert np.array_equal(got_pos, pos)
+    small = rng.integers(0, 7, size=333).astype(np.int32)
+    got_pos, got_off = _static_plan(torch, small, P)
+    pos, off = _expected_plan(small, P)
+    assert np.array_equal(got_off, off)
+    assert np.array_equal(got_pos, pos)
+    assert got_off[-1] == off[7] and np.all(got_off[7:] == got_off[7])
