@@ -283,6 +283,74 @@ MM_API mm_status mm_profile_end(mm_handle h, float *ms_out, int max_out, int *n_
 MM_API mm_status mm_plan_dispatch_static(const int32_t *phys, int64_t npairs, int num_physical, int32_t *pos,
                                          int32_t *offsets, mm_stream stream);
 
+/* ---- Expert parallelism across ranks -------------------------------------
+ * The pages run the fused operator expert-parallel over eight GPUs, with
+ * all-to-all dispatch and combine buffers ("sglang PR #35619", launch
+ * settings; "sglang PR #47065", Title/switches: one kernel covers quantisation,
+ * dispatch, both expert GEMMs and the combine across ranks).  Here the P
+ * physical experts are split over `world` ranks in contiguous ranges, each
+ * rank one handle on its own GPU, and one rank's forward is:
+ *
+ *   mm_ep_dispatch   its tokens -> send buffer, rows grouped by destination
+ *   (caller)         all-to-all: rank d receives its range from every rank
+ *   mm_ep_experts    received rows -> y rows, in the order received
+ *   (caller)         all-to-all back: y rows return to the sending rank
+ *   mm_ep_combine    y rows in send order -> the layer output
+ *
+ * Row arithmetic is that of mm_forward (same codes, scales, MMAs, epilogue and
+ * combine order), so the output equals the single-GPU forward's bit for bit.
+ *
+ * mm_set_expert_parallel: make this handle rank `rank` of `world`; first
+ * (host, [world + 1]) gives each rank's range [first[r], first[r+1]) of
+ * physical experts, first[0] = 0, first[world] = P, every range non-empty.
+ * Afterwards mm_set_weights takes the weights of the rank's own experts only
+ * ([first[rank+1] - first[rank]] experts, the same layouts), the routing and
+ * the EPLB map stay global, and mm_forward, mm_rebalance, shared experts and
+ * the a16w4 format return MM_ERR_UNSUPPORTED.  Frees the weights and the
+ * workspace.  Synchronous; not during capture. */
+MM_API mm_status mm_set_expert_parallel(mm_handle h, int rank, int world, const int32_t *first);
+
+/* Workspace for dispatching up to max_tokens of this rank's tokens and for
+ * receiving up to max_recv_rows rows (padding rows included).  Allocates;
+ * call before capture. */
+MM_API mm_status mm_ep_reserve(mm_handle h, int64_t max_tokens, int64_t max_recv_rows);
+
+/* Rows the send buffers need for num_tokens tokens: T k pairs plus the
+ * padding of each expert's segment to a multiple of 16 rows. */
+MM_API mm_status mm_ep_send_rows(mm_handle h, int64_t num_tokens, int64_t *rows);
+
+/* Step 1, on the source rank.  hidden [T, H] bf16, logits [T, E] fp32 and
+ * bias [E] fp32 (or NULL) as in mm_forward.  Writes, for rows = the value of
+ * mm_ep_send_rows (caller-owned device buffers, 16-byte aligned):
+ *   send_xq  [rows, H]     e4m3 codes of each (token, slot) pair
+ *   send_xs  [rows, H/32]  their e8m0 scales, row-major
+ *   send_eid [rows] int32  the pair's expert index among its destination
+ *                          rank's experts; -1 on a padding row
+ * Rows bound for rank d are [row_off[d], row_off[d+1]) (row_off: host,
+ * [world + 1], written by this call); inside that range the segments of d's
+ * experts in expert order, pairs in (token, slot) order, each segment padded
+ * to 16 rows.  Records counts as mm_forward does.  Synchronous at its end (it
+ * reads the split sizes back for the all-to-all), so not capturable.
+ * T > reserved tokens -> MM_ERR_CAPACITY; T == 0 -> all row_off 0. */
+MM_API mm_status mm_ep_dispatch(mm_handle h, const void *hidden, const float *logits, const float *bias,
+                                int64_t num_tokens, void *send_xq, void *send_xs, int32_t *send_eid,
+                                int64_t *row_off, mm_stream stream);
+
+/* Step 2, on the destination rank.  recv_xq [n, H], recv_xs [n, H/32] and
+ * recv_eid [n] are the rows this rank received (in any order of sources;
+ * padding rows, eid -1, are skipped).  Writes y_recv [n, H] bf16: row i is
+ * GEMM2(SwiGLU(GEMM1(row i))) of expert recv_eid[i], zeros for a padding
+ * row.  Asynchronous on `stream`; allocates nothing.  n > reserved receive
+ * rows -> MM_ERR_CAPACITY; weights not set -> MM_ERR_NOT_READY. */
+MM_API mm_status mm_ep_experts(mm_handle h, const void *recv_xq, const void *recv_xs, const int32_t *recv_eid,
+                               int64_t n, void *y_recv, mm_stream stream);
+
+/* Step 3, on the source rank: y_back [rows, H] bf16 holds the y rows returned
+ * by the destinations in send-buffer order (rows of the last mm_ep_dispatch);
+ * out [T, H] bf16 = sum_j w[t,j] y_back[row of (t, j)] over that dispatch's
+ * tokens, fp32 in slot order.  Asynchronous; allocates nothing. */
+MM_API mm_status mm_ep_combine(mm_handle h, const void *y_back, void *out, mm_stream stream);
+
 /* Short text for a status code (static storage). */
 MM_API const char *mm_status_string(mm_status s);
 

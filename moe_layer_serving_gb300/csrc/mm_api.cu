@@ -164,6 +164,9 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
         const char* f = getenv("MM_FAULT");
         if (f && !strcmp(f, "grid_barrier")) c->fault = mm::kFaultGridBarrier;
         else if (f && !strcmp(f, "gemm_dependency")) c->fault = mm::kFaultGemmDependency;
+#ifdef MM_DEBUG
+        else if (f && !strcmp(f, "map_entry")) c->fault = mm::kFaultMapEntry;
+#endif
     }
     c->small_max = env_int("MM_SMALL_M_MAX", mm::kSmallMaxTokens);
     if (c->small_max > mm::kSmallMaxTokens) c->small_max = mm::kSmallMaxTokens;
@@ -198,6 +201,7 @@ mm_status mm_destroy(mm_handle c)
     cudaGetLastError();
     free_ws(c);
     profile_free(c);
+    mm::ep_release(c);
     void* ptrs[] = {c->w1, c->w1_sf, c->w2, c->w2_sf, c->map, c->rc, c->counts, c->status};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -210,7 +214,7 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
     if (!c || !w1 || !w1s || !w2 || !w2s) return MM_ERR_INVALID_ARG;
     if (!aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1s, 16) || !aligned(w2s, 16)) return MM_ERR_INVALID_ARG;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
-    const size_t P = mm::pw(c), H = c->H, I = c->I;      // routed and shared physical experts
+    const size_t P = mm::wexp(c), H = c->H, I = c->I;    // the physical experts this handle holds
     const mm::WOrder o1 = mm::w1_order(c->H, c->I), o2 = mm::w2_order(c->H, c->I);
     const size_t b1 = mm::w_blocks(o1, static_cast<int>(P)), b2 = mm::w_blocks(o2, static_cast<int>(P));
     const size_t n_w1 = b1 * 8192, n_w1s = b1 * 512;
@@ -284,6 +288,19 @@ mm_status mm_set_eplb_map(mm_handle c, const int32_t* pol, const int32_t* rc, in
         cudaFree(drc);
         return MM_ERR_CUDA;
     }
+#ifdef MM_DEBUG
+    if (c->fault == mm::kFaultMapEntry) {
+        // the validated map's entry (logical 0, replica 0) overwritten on the
+        // device with a physical id past the last expert
+        const int32_t bad = c->P + 7;
+        if (cudaMemcpy(dm, &bad, sizeof(bad), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(dm);
+            cudaFree(drc);
+            return MM_ERR_CUDA;
+        }
+    }
+#endif
     cudaDeviceSynchronize();
     if (c->map) cudaFree(c->map);
     if (c->rc) cudaFree(c->rc);
@@ -329,6 +346,7 @@ mm_status mm_plan_replicas(const int64_t* load, int E, int P, int max_replicas, 
 mm_status mm_rebalance(mm_handle c, int layer, int max_replicas)
 {
     if (!c || layer < 0 || layer >= MM_MAX_LAYERS || max_replicas < 1) return MM_ERR_INVALID_ARG;
+    if (c->ep) return MM_ERR_UNSUPPORTED;
     if (!c->weights_set || !c->map_set) return MM_ERR_NOT_READY;
     if (c->P == c->E) return MM_OK;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
@@ -387,6 +405,7 @@ mm_status mm_set_activation_format(mm_handle c, mm_act act)
 {
     if (!c || (act != MM_ACT_MXFP8 && act != MM_ACT_BF16)) return MM_ERR_INVALID_ARG;
     if (act == c->act) return MM_OK;
+    if (c->ep) return MM_ERR_UNSUPPORTED;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
     cudaDeviceSynchronize();
     free_ws(c);
@@ -401,6 +420,7 @@ mm_status mm_set_shared_experts(mm_handle c, int num_shared)
     if (!c || num_shared < 0 || c->k + num_shared > MM_MAX_TOPK || c->P + num_shared > MM_MAX_EXPERTS)
         return MM_ERR_INVALID_ARG;
     if (num_shared == c->ns) return MM_OK;
+    if (c->ep) return MM_ERR_UNSUPPORTED;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
     cudaDeviceSynchronize();
     // every per-expert and per-pair size changes: weights and workspace go
@@ -423,8 +443,17 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     if (!c || max_tokens < 0 || max_tokens > (int64_t(1) << 24)) return MM_ERR_INVALID_ARG;
     if (max_tokens <= c->cap_tokens) return MM_OK;
     if (capturing(nullptr)) return MM_ERR_INVALID_ARG;
+    return mm::reserve_pairs(c, max_tokens * mm::slots(c), max_tokens);
+}
+
+}  // extern "C"
+
+// The workspace for up to `npairs` (token, slot) pairs -- or received rows
+// under expert parallelism -- over the routing's physical experts, and for
+// forwards of up to `max_tokens` tokens.
+mm_status mm::reserve_pairs(mm_handle c, int64_t npairs, int64_t max_tokens)
+{
     const int kk = mm::slots(c), P = mm::pw(c);              // slots per token, physical experts
-    const int64_t npairs = max_tokens * kk;
     // each non-empty segment adds < kSegAlign pad rows and < 1 partial token tile
     const int64_t busy = npairs < P ? npairs : P;
     const int64_t rows = npairs + busy * (mm::kSegAlign - 1) + mm::kSegAlign;
@@ -505,10 +534,13 @@ mm_status mm_reserve(mm_handle c, int64_t max_tokens)
     return MM_OK;
 }
 
+extern "C" {
+
 mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const float* bias, void* out,
                      int64_t T, mm_stream stream)
 {
     if (!c || T < 0) return MM_ERR_INVALID_ARG;
+    if (c->ep) return MM_ERR_UNSUPPORTED;       // an expert-parallel rank runs mm_ep_dispatch / _experts / _combine
     if (!c->weights_set || !c->map_set) return MM_ERR_NOT_READY;
     if (T == 0) return MM_OK;
     if (!hidden || !logits || !out) return MM_ERR_INVALID_ARG;

@@ -38,6 +38,21 @@ __device__ __forceinline__ void latch_error(int* status, int code, int site = 0)
     if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, site);
 }
 
+// Bounds checks of debug builds (compiled with MM_DEBUG): MM_CHECK(cond,
+// status, site) is cond, and when cond is false it latches MM_ERR_DEVICE
+// with the site, so the caller skips the access it guards.  In release builds
+// it is the constant true and every check compiles away.
+#ifdef MM_DEBUG
+__device__ __forceinline__ bool debug_check(bool ok, int* status, int site)
+{
+    if (!ok) latch_error(status, MM_ERR_DEVICE, site);
+    return ok;
+}
+#define MM_CHECK(cond, status, site) (::mm::debug_check((cond), (status), (site)))
+#else
+#define MM_CHECK(cond, status, site) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

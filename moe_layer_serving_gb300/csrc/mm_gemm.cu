@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tv.row0 = g.tile_row0;
     tv.rows = g.tile_rows;
     tv.ntiles = *g.num_tiles;
+    tv.first = g.tile_first;
+    tv.experts = g.P;
     gemm_roles<Geo>(maps, g, tv, s, tmem);
     gemm_teardown(tmem);
 }
@@ -52,14 +54,16 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.tile_row0 = c->tile_row0;
     g.tile_rows = c->tile_rows;
     g.num_tiles = c->num_tiles;
+    g.tile_first = c->toff;
     g.done1 = c->done1;
     g.unit_next = c->unit_next;
     g.status = c->status;
     g.H = c->H;
     g.I = c->I;
-    g.P = pw(c);
+    g.P = wexp(c);
     g.phases = 3;
     g.fault = c->fault;
+    g.rows_cap = static_cast<int>(c->rows_cap);
 }
 
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)

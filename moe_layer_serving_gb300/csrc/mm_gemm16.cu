@@ -168,6 +168,10 @@ __device__ __forceinline__ bool decode16(const Gemm16Args& g, int u, Unit16& un)
     un.expert = g.tile_expert[un.tile];
     un.row0 = g.tile_row0[un.tile];
     un.rows = g.tile_rows[un.tile];
+    if (!MM_CHECK(un.expert >= 0 && un.expert < g.P && un.row0 >= 0 && un.rows >= 1 && un.rows <= 128 &&
+                      un.row0 + un.rows <= g.rows_cap,
+                  g.status, kSiteGemmTile))
+        return false;
     un.n = (un.rows + 15) & ~15;
     un.tbox = un.rows <= 16 ? 0 : (un.rows <= 32 ? 1 : (un.rows <= 64 ? 2 : 3));
     if (un.phase == 1) {
@@ -759,6 +763,8 @@ cudaError_t launch_gemm16(const mm_ctx* c, cudaStream_t s)
     g.H = c->H;
     g.I = c->I;
     g.fault = c->fault;
+    g.P = wexp(c);
+    g.rows_cap = static_cast<int>(c->rows_cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c->sms));
     cfg.blockDim = dim3(kT16Threads);

@@ -141,6 +141,7 @@ struct Gemm16Args {
     int* status;
     int H, I;
     int fault;
+    int P, rows_cap;        // bounds checks of debug builds
 };
 
 struct GemmArgs {
@@ -156,12 +157,14 @@ struct GemmArgs {
     const int* tile_row0;
     const int* tile_rows;
     const int* num_tiles;
+    const int* tile_first;  // per expert: its first token tile
     int* done1;             // per token tile: GEMM1 units finished
     int* unit_next;         // next unit to hand out (zeroed before the GEMM phase)
     int* status;
     int H, I, P;
     int phases;             // bit 0: GEMM1 units, bit 1: GEMM2 units
     int fault;              // injected fault (FaultSite), 0 = none
+    int rows_cap;           // dispatch rows reserved (bounds checks of debug builds)
 };
 
 }  // namespace mm
@@ -205,6 +208,17 @@ struct mm_ctx {
     // per-launch timing of the dominant kernel: event pairs, pairs recorded so far
     std::vector<cudaEvent_t> prof_events;
     int prof_used = 0;
+    // expert parallelism (mm_set_expert_parallel): this handle is rank ep_rank
+    // of ep_world and holds the weights of physical experts
+    // [ep_first[ep_rank], ep_first[ep_rank + 1]), ep_local of them
+    bool ep = false;
+    int ep_rank = 0, ep_world = 1, ep_local = 0;
+    std::vector<int32_t> ep_first;     // [world + 1]
+    int32_t* ep_local_id = nullptr;    // [P] device: index of each physical expert among its owner's
+    int32_t* ep_recv_pos = nullptr;    // [ep_recv_cap] dispatch row of each received row
+    int64_t ep_recv_cap = 0;
+    int64_t ep_T = 0;                  // tokens of the last mm_ep_dispatch
+    int64_t ep_send_rows = 0;          // send-buffer rows of the last mm_ep_dispatch
     // last forward (debug dumps)
     int last_route = 0, last_launches = 0, last_site = 0;
     int64_t last_T = 0;
@@ -222,6 +236,12 @@ enum WaitSite {
     kSiteProducerDone1 = 5,
     kSiteGridBarrier = 6,
     kSiteUnitQueue = 7,
+    // sites of a failed device-side bounds check (debug builds, MM_ERR_DEVICE)
+    kSiteRouteMap = 8,       // EPLB map entry or replica count outside its range
+    kSitePermute = 9,        // a pair's physical expert outside [0, P) at the permute
+    kSiteDispatch = 10,      // dispatch row or physical expert out of range at the quantise/dispatch copy
+    kSiteGemmTile = 11,      // token tile with an expert or rows outside the reserved workspace
+    kSiteCombine = 12,       // dispatch row outside the reserved rows at the combine
 };
 
 // Fault injection for the failure-detection tests (environment variable
@@ -231,17 +251,29 @@ enum WaitSite {
 enum FaultSite {
     kFaultNone = 0,
     kFaultGridBarrier = 1,   // CTA 0 withholds its arrival at the fused kernel's second grid barrier
-    kFaultGemmDependency = 2 // GEMM2 units wait for one GEMM1 unit more than a tile has
+    kFaultGemmDependency = 2, // GEMM2 units wait for one GEMM1 unit more than a tile has
+    // Debug builds only (MM_DEBUG): after mm_set_eplb_map has validated and
+    // uploaded the map, one device map entry is overwritten with a physical id
+    // past the last expert.  The route's bounds check must catch it before any
+    // later stage indexes with it; a release build ignores this fault, since
+    // without the checks the id would be used as an index.
+    kFaultMapEntry = 3
 };
 
 // host-side launchers (return cudaGetLastError of the launch)
-// slots per token (k routed + the shared experts) and physical experts with
-// weights (P routed + the shared experts)
+// slots per token (k routed + the shared experts) and physical experts of the
+// routing (P routed + the shared experts)
 inline int slots(const mm_ctx* c) { return c->k + c->ns; }
 inline int pw(const mm_ctx* c) { return c->P + c->ns; }
+// physical experts whose weights this handle holds: all of them, or under
+// expert parallelism the rank's own range
+inline int wexp(const mm_ctx* c) { return c->ep ? c->ep_local : c->P + c->ns; }
 
 cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias, int64_t T, cudaStream_t s);
 cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s);
+// the same permute over any ids (negative ids left out) into pos
+cudaError_t launch_permute_ids(const mm_ctx* c, const int32_t* ids, int64_t npairs, int P, int32_t* pos,
+                               cudaStream_t s);
 cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s);
 cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s);
@@ -255,5 +287,7 @@ cudaError_t small_prepare();
 cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logits, const float* bias, void* out,
                          int64_t T, cudaStream_t s);
 void fill_gemm_args(const mm_ctx* c, GemmArgs* g);
+mm_status reserve_pairs(mm_ctx* c, int64_t npairs, int64_t max_tokens);
+void ep_release(mm_ctx* c);    // frees the expert-parallel buffers
 
 }  // namespace mm

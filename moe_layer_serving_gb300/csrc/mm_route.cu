@@ -38,15 +38,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a)
 // permute: chunk histograms -> per-expert scan (segments padded to 16 rows,
 // token tiles of up to 128 rows) -> stable scatter (pairs keep (token, slot) order)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) hist_kernel(const int32_t* phys, int64_t npairs, int P, int32_t* chunk_hist)
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* phys, int64_t npairs, int P, int32_t* chunk_hist,
+                                                   int* status)
 {
+    (void)status;
     __shared__ int hist[MM_MAX_EXPERTS];
     for (int p = threadIdx.x; p < P; p += blockDim.x) hist[p] = 0;
     __syncthreads();
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunkPairs;
     for (int i = threadIdx.x; i < kChunkPairs; i += blockDim.x) {
         const int64_t g = base + i;
-        if (g < npairs) atomicAdd(&hist[phys[g]], 1);
+        if (g < npairs) {
+            // a negative id is a row to leave out (a padding row received
+            // from another rank); ids at or past P are errors
+            const int p = phys[g];
+            if (p >= 0 && MM_CHECK(p < P, status, kSitePermute)) atomicAdd(&hist[p], 1);
+        }
     }
     __syncthreads();
     for (int p = threadIdx.x; p < P; p += blockDim.x) chunk_hist[static_cast<int64_t>(blockIdx.x) * P + p] = hist[p];
@@ -142,6 +149,18 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
 constexpr int kScatterWarps = 8;
 static_assert(kChunkPairs % (32 * kScatterWarps) == 0, "a chunk splits evenly over the warps");
 
+// (Debug builds: a physical id outside [0, P) -- already reported by the
+// histogram -- is left out like a pair past the end.)
+__device__ __forceinline__ int scatter_id(const int32_t* phys, int64_t i, int64_t npairs, int P)
+{
+    int p = i < npairs ? phys[i] : -1;
+#ifdef MM_DEBUG
+    if (p >= P) p = -1;
+#endif
+    (void)P;
+    return p;
+}
+
 __global__ void __launch_bounds__(32 * kScatterWarps) scatter_kernel(const int32_t* phys, int64_t npairs, int P,
                                                                      const int32_t* chunk_base, const int32_t* off,
                                                                      int32_t* pos)
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(32 * kScatterWarps) scatter_kernel(const int32
     const uint32_t lt = (1u << lane) - 1u;
     for (int it = 0; it < kPer / 32; ++it) {
         const int64_t i = base + it * 32 + lane;
-        const int p = i < npairs ? phys[i] : -1;
+        const int p = scatter_id(phys, i, npairs, P);
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
         if (p >= 0 && lane == __ffs(peers) - 1) wcnt[w][p] += __popc(peers);
         __syncwarp();
@@ -173,7 +192,7 @@ __global__ void __launch_bounds__(32 * kScatterWarps) scatter_kernel(const int32
     __syncthreads();
     for (int it = 0; it < kPer / 32; ++it) {
         const int64_t i = base + it * 32 + lane;
-        const int p = i < npairs ? phys[i] : -1;
+        const int p = scatter_id(phys, i, npairs, P);
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, p);
         int before = 0;
         if (p >= 0) {
@@ -196,20 +215,22 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(const __nv_bfloat16
                                                             const int32_t* __restrict__ phys,
                                                             const int32_t* __restrict__ off,
                                                             const int32_t* __restrict__ toff,
-                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t)
+                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t,
+                                                            DispatchBounds chk)
 {
     const int nb = H / 32;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = g / nb;
     if (t >= T) return;
     quant_dispatch_block(x, t, static_cast<int>(g % nb), H, k, pos + t * k, phys + t * k, off, toff, kTokTile, xq,
-                         xs_t);
+                         xs_t, chk);
 }
 
 // a16w4 dispatch: token t's bf16 row copied to its k dispatch rows; one thread
 // per 16-byte chunk (one load, k stores).
 __global__ void __launch_bounds__(256) dispatch16_kernel(const uint4* __restrict__ x, int64_t T, int H, int k,
-                                                         const int32_t* __restrict__ pos, uint4* __restrict__ xd)
+                                                         const int32_t* __restrict__ pos, uint4* __restrict__ xd,
+                                                         DispatchBounds chk)
 {
     const int nc = H / 8;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -217,7 +238,10 @@ __global__ void __launch_bounds__(256) dispatch16_kernel(const uint4* __restrict
     if (t >= T) return;
     const int c = static_cast<int>(g % nc);
     const uint4 v = x[t * nc + c];
-    for (int j = 0; j < k; ++j) xd[static_cast<int64_t>(pos[t * k + j]) * nc + c] = v;
+    for (int j = 0; j < k; ++j) {
+        const int64_t row = pos[t * k + j];
+        if (MM_CHECK(row >= 0 && row < chk.rows_cap, chk.status, kSiteDispatch)) xd[row * nc + c] = v;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -226,13 +250,13 @@ __global__ void __launch_bounds__(256) dispatch16_kernel(const uint4* __restrict
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w,
                                                      const int32_t* __restrict__ pos, int64_t T, int H, int k,
-                                                     __nv_bfloat16* __restrict__ out)
+                                                     __nv_bfloat16* __restrict__ out, DispatchBounds chk)
 {
     const int nc = H / 8;
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = g / nc;
     if (t >= T) return;
-    combine_chunk(y, w, pos, t, static_cast<int>(g % nc), H, k, out);
+    combine_chunk(y, w, pos, t, static_cast<int>(g % nc), H, k, out, chk);
 }
 
 __global__ void tile_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows, int K,
@@ -260,6 +284,8 @@ __global__ void tile_weights_kernel(const uint4* __restrict__ src, uint8_t* __re
 
 unsigned grid_for(int64_t threads, int block) { return static_cast<unsigned>((threads + block - 1) / block); }
 
+DispatchBounds bounds_of(const mm_ctx* c) { return DispatchBounds{pw(c), c->rows_cap, c->status}; }
+
 }  // namespace
 
 cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias, int64_t T, cudaStream_t s)
@@ -279,19 +305,25 @@ cudaError_t launch_route(const mm_ctx* c, const float* logits, const float* bias
     a.R = c->R;
     a.ns = c->ns;
     a.P = c->P;
+    a.status = c->status;
     route_kernel<<<grid_for(T, kRouteWarps), kRouteWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
 {
-    const int64_t npairs = T * slots(c);
+    return launch_permute_ids(c, c->phys, T * slots(c), pw(c), c->pos, s);
+}
+
+cudaError_t launch_permute_ids(const mm_ctx* c, const int32_t* ids, int64_t npairs, int P, int32_t* pos,
+                               cudaStream_t s)
+{
     const int nchunks = static_cast<int>((npairs + kChunkPairs - 1) / kChunkPairs);
-    hist_kernel<<<nchunks, 256, 0, s>>>(c->phys, npairs, pw(c), c->chunk_hist);
+    hist_kernel<<<nchunks, 256, 0, s>>>(ids, npairs, P, c->chunk_hist, c->status);
     ScanArgs a;
     a.chunk_hist = c->chunk_hist;
     a.nchunks = nchunks;
-    a.P = pw(c);
+    a.P = P;
     a.off = c->off;
     a.toff = c->toff;
     a.tile_expert = c->tile_expert;
@@ -300,7 +332,7 @@ cudaError_t launch_permute(const mm_ctx* c, int64_t T, cudaStream_t s)
     a.num_tiles = c->num_tiles;
     a.done1 = c->done1;
     scan_kernel<<<1, 512, 0, s>>>(a);
-    scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(c->phys, npairs, pw(c), c->chunk_hist, c->off, c->pos);
+    scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(ids, npairs, P, c->chunk_hist, c->off, pos);
     return cudaGetLastError();
 }
 
@@ -309,7 +341,7 @@ cudaError_t launch_quant_dispatch(const mm_ctx* c, const void* hidden, int64_t T
     const int64_t threads = T * (c->H / 32);
     quant_dispatch_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hidden), T, c->H,
                                                                  slots(c), c->pos, c->phys, c->off, c->toff, c->xq,
-                                                                 c->xs_t);
+                                                                 c->xs_t, bounds_of(c));
     return cudaGetLastError();
 }
 
@@ -317,7 +349,7 @@ cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cu
 {
     const int64_t threads = T * (c->H / 8);
     dispatch16_kernel<<<grid_for(threads, 256), 256, 0, s>>>(static_cast<const uint4*>(hidden), T, c->H, slots(c),
-                                                             c->pos, reinterpret_cast<uint4*>(c->xq));
+                                                             c->pos, reinterpret_cast<uint4*>(c->xq), bounds_of(c));
     return cudaGetLastError();
 }
 
@@ -325,7 +357,7 @@ cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s
 {
     const int64_t threads = T * (c->H / 8);
     combine_kernel<<<grid_for(threads, 256), 256, 0, s>>>(c->y, c->wgt, c->pos, T, c->H, slots(c),
-                                                          static_cast<__nv_bfloat16*>(out));
+                                                          static_cast<__nv_bfloat16*>(out), bounds_of(c));
     return cudaGetLastError();
 }
 

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t T = a.route.T;
     const int k = a.route.k + a.route.ns, P = a.P, H = g.H;     // slots per token, physical experts
     const int N = static_cast<int>(T) * k;
+    const DispatchBounds chk{P, g.rows_cap, g.status};
     uint64_t* stamp = a.stamps + static_cast<int64_t>(blockIdx.x) * 8;
     if (threadIdx.x == 0) stamp[0] = globaltimer();
 
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
              it += static_cast<int64_t>(gridDim.x) * kThreads) {
             const int64_t t = it / nb;
             quant_dispatch_block(a.x, t, static_cast<int>(it % nb), H, k, spos + t * k, sphys + t * k, soff, stoff,
-                                 tile, a.xq, a.xs_t);
+                                 tile, a.xq, a.xs_t, chk);
         }
         fence_proxy_async_global();
     }
@@ -325,6 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tv.row0 = t_row0;
         tv.rows = t_rows;
         tv.ntiles = scal[0];
+        tv.first = nullptr;         // a few tiles per expert: tile by tile
+        tv.experts = P;
         if (short_tiles)
             gemm_roles<GeomSmall>(maps, g, tv, s, tmem);
         else
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nc = H / 8;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < T * nc;
              it += static_cast<int64_t>(gridDim.x) * kThreads)
-            combine_chunk(g.y, a.route.w, a.pos, it / nc, static_cast<int>(it % nc), H, k, a.out);
+            combine_chunk(g.y, a.route.w, a.pos, it / nc, static_cast<int>(it % nc), H, k, a.out, chk);
     }
     __syncthreads();
     if (threadIdx.x == 0) stamp[7] = globaltimer();
@@ -376,6 +379,7 @@ cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logit
     a.route.ns = c->ns;
     a.route.P = c->P;
     a.route.R = c->R;
+    a.route.status = c->status;
     a.x = static_cast<const __nv_bfloat16*>(hidden);
     a.out = static_cast<__nv_bfloat16*>(out);
     a.pos = c->pos;

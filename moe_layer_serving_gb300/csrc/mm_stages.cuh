@@ -63,6 +63,7 @@ struct RouteArgs {
     int64_t T;
     int E, k, R;
     int ns, P;             // fused shared experts: slot k + s -> physical P + s, weight 1
+    int* status;           // latched device status (bounds checks of debug builds)
 };
 
 // Order-preserving map of a binary32 key to uint32 (larger key, larger code).
@@ -140,10 +141,18 @@ __device__ __forceinline__ void route_token(const RouteArgs& a, int64_t t, int l
     const int kk = a.k + a.ns;
     if (lane < a.k) {
         const int e = my_e;
-        const uint32_t slot = static_cast<uint32_t>(t + lane) % static_cast<uint32_t>(a.rc[e]);
+        const int rc = a.rc[e];
+        int p = -1;
+        if (MM_CHECK(rc >= 1 && rc <= a.R, a.status, kSiteRouteMap)) {
+            const uint32_t slot = static_cast<uint32_t>(t + lane) % static_cast<uint32_t>(rc);
+            p = a.map[e * a.R + static_cast<int>(slot)];
+        }
+        // a map entry outside [0, P) is recorded and replaced by -1, which
+        // every later stage of a debug build leaves out
+        if (!MM_CHECK(p >= 0 && p < a.P, a.status, kSiteRouteMap)) p = -1;
         a.idx[t * kk + lane] = e;
         a.w[t * kk + lane] = __fdiv_rn(my_s, S);
-        a.phys[t * kk + lane] = a.map[e * a.R + static_cast<int>(slot)];
+        a.phys[t * kk + lane] = p;
         if (a.counts) {
             if (hist) atomicAdd(&hist[e], 1);
             else atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + e), 1ull);
@@ -164,16 +173,18 @@ __device__ __forceinline__ void route_token_any(const RouteArgs& a, int64_t t, i
     else route_token<16>(a, t, lane, hist);
 }
 
-// MXFP8 quantisation of block b (32 elements) of token t and its dispatch to
-// the token's k rows: 4 x 128-bit loads, one e8m0 scale, 32 e4m3 codes per
-// row (2 x 128-bit stores).  pos_t / phys_t: the k dispatch rows and physical
-// experts of token t; off / toff: segment start row and first token tile of
-// each expert (global or shared memory), which place the scale byte in the
-// scale tile of the row's token tile.
-__device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
-                                                     int k, const int32_t* pos_t, const int32_t* phys_t,
-                                                     const int32_t* off, const int32_t* toff, int tile,
-                                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t)
+// The bounds of a debug build's checks (unused otherwise).
+struct DispatchBounds {
+    int P;              // physical experts with weights
+    int64_t rows_cap;   // dispatch rows reserved
+    int* status;
+};
+
+// MXFP8 quantisation of block b (32 elements) of token t: 4 x 128-bit loads;
+// the 32 e4m3 codes packed four to a word, and the e8m0 scale byte as the
+// return value.
+__device__ __forceinline__ uint8_t quant_block32(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
+                                                uint32_t (&packed)[8])
 {
     const uint4* src = reinterpret_cast<const uint4*>(x + t * H + b * 32);
     float v[32];
@@ -192,7 +203,6 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
     const int X = mx_e4m3_exponent(amax);
     const float inv = exp2i(-X);
-    uint32_t packed[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         uint32_t wd = 0;
@@ -202,14 +212,31 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
         }
         packed[i] = wd;
     }
-    const uint8_t sbyte = static_cast<uint8_t>(X + 127);
+    return static_cast<uint8_t>(X + 127);
+}
+
+// MXFP8 quantisation of block b of token t and its dispatch to the token's k
+// rows: 32 e4m3 codes per row (2 x 128-bit stores).  pos_t / phys_t: the k
+// dispatch rows and physical experts of token t; off / toff: segment start row
+// and first token tile of each expert (global or shared memory), which place
+// the scale byte in the scale tile of the row's token tile.
+__device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
+                                                     int k, const int32_t* pos_t, const int32_t* phys_t,
+                                                     const int32_t* off, const int32_t* toff, int tile,
+                                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_t,
+                                                     const DispatchBounds& chk)
+{
+    (void)chk;
+    uint32_t packed[8];
+    const uint8_t sbyte = quant_block32(x, t, b, H, packed);
     const int kchunks = H / 128;
     for (int j = 0; j < k; ++j) {
         const int64_t row = pos_t[j];
+        const int p = phys_t[j];
+        if (!MM_CHECK(p >= 0 && p < chk.P && row >= 0 && row < chk.rows_cap, chk.status, kSiteDispatch)) continue;
         uint4* dst = reinterpret_cast<uint4*>(xq + row * H + b * 32);
         dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        const int p = phys_t[j];
         const int rank = static_cast<int>(row) - off[p];
         xs_t[act_sf_offset(toff[p] + rank / tile, rank % tile, b, kchunks)] = sbyte;
     }
@@ -220,8 +247,9 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
 // 16-byte reads in flight instead of one.
 __device__ __forceinline__ void combine_chunk(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w,
                                               const int32_t* __restrict__ pos, int64_t t, int c, int H, int k,
-                                              __nv_bfloat16* __restrict__ out)
+                                              __nv_bfloat16* __restrict__ out, const DispatchBounds& chk)
 {
+    (void)chk;
     float wj[MM_MAX_TOPK];
     uint4 u[MM_MAX_TOPK];
 #pragma unroll
@@ -229,7 +257,10 @@ __device__ __forceinline__ void combine_chunk(const __nv_bfloat16* __restrict__ 
         if (j < k) {
             wj[j] = w[t * k + j];
             const int64_t row = pos[t * k + j];
-            u[j] = *(reinterpret_cast<const uint4*>(y + row * H) + c);
+            if (MM_CHECK(row >= 0 && row < chk.rows_cap, chk.status, kSiteCombine))
+                u[j] = *(reinterpret_cast<const uint4*>(y + row * H) + c);
+            else
+                u[j] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     float acc[8];

@@ -34,6 +34,15 @@ def test_library_exports_every_declared_symbol(built):
     assert not missing, missing
 
 
+def test_debug_library_exports_every_declared_symbol(built):
+    # the build with device-side bounds checks: the same entry points
+    from moe_layer_serving_gb300 import build
+    assert os.path.exists(build.DEBUG_LIB)
+    lib = C.CDLL(build.DEBUG_LIB)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
 def test_binding_exposes_c_names(built):
     import moe_layer_serving_gb300 as mm
     for n in _declared():
@@ -71,6 +80,9 @@ def test_null_handle_calls_are_invalid(built):
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import moe_layer_serving_gb300 as mm
     monkeypatch.setattr(mm, "library_path", str(tmp_path / "absent.so"))
-    monkeypatch.setattr(mm, "_lib", None)
+    monkeypatch.setattr(mm, "debug_library_path", str(tmp_path / "absent_debug.so"))
+    monkeypatch.setattr(mm, "_libs", {})
     with pytest.raises(RuntimeError, match="missing"):
         mm.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        mm.lib(debug=True)

@@ -108,3 +108,76 @@ def test_forward_after_unread_failure_does_no_work(torch):
     assert run.op.last_info()[2] == SITE_GRID_BARRIER
     assert run.op.get_status() == 0                  # read and cleared
     run.close()
+
+
+SITE_ROUTE_MAP = 8
+
+
+@pytest.mark.parametrize("route", [1, 2])
+def test_corrupt_map_entry_is_caught_at_the_route_in_the_debug_build(torch, route):
+    # The build with device-side bounds checks (libmegamoe_debug.so): after
+    # mm_set_eplb_map validated the map, MM_FAULT=map_entry overwrites the
+    # device entry of logical expert 0 with a physical id past the last expert.
+    # The route's check must catch it before any later stage indexes with it:
+    # MM_ERR_DEVICE with the route's site, the pairs of expert 0 left out
+    # (physical id -1), every other pair placed as the oracle places it.
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    T = 64
+    hidden, logits, bias = synthetic.make_activations(cfg, T)
+    idx, _ = oracle.route(logits, bias, cfg.k)
+    assert (idx == 0).any()
+    os.environ["MM_FAULT"] = "map_entry"
+    try:
+        op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I, debug=True)
+    finally:
+        del os.environ["MM_FAULT"]
+    dev = torch.device("cuda:0")
+    op.set_weights(*[torch.from_numpy(a).to(dev) for a in gpu_util.weights(cfg)])
+    op.reserve(T)
+    op.set_route(mm.ROUTE_SMALL if route == 1 else mm.ROUTE_LARGE)
+    x = torch.from_numpy(hidden.view(np.int16)).to(dev).view(torch.bfloat16)
+    lg, b = torch.from_numpy(logits).to(dev), torch.from_numpy(bias).to(dev)
+    out = torch.empty_like(x)
+    op.forward(x, lg, b, out)
+    torch.cuda.synchronize()
+    assert op.last_info()[0] == route
+    phys = op.debug_dump(2).reshape(T, cfg.k)
+    assert op.get_status() == mm.MM_ERR_DEVICE
+    assert op.last_info()[2] == SITE_ROUTE_MAP
+    assert np.array_equal(phys == -1, idx == 0)
+    assert np.array_equal(phys[idx != 0], idx[idx != 0])        # identity map elsewhere
+    op.close()
+
+
+@pytest.mark.parametrize("route", [1, 2])
+def test_debug_build_runs_the_layer_and_release_ignores_the_debug_fault(torch, route):
+    # without a fault the bounds-checked build computes the same layer; the
+    # release build ignores MM_FAULT=map_entry (it has no checks to catch it)
+    import moe_layer_serving_gb300 as mm
+    cfg = synthetic.CONFIGS[0]
+    T = 64
+    hidden, logits, bias = synthetic.make_activations(cfg, T)
+    ref = oracle.forward(hidden, logits, bias, cfg.k, gpu_util.weights(cfg))
+    dev = torch.device("cuda:0")
+    outs = []
+    for debug, fault in ((True, None), (False, "map_entry")):
+        if fault:
+            os.environ["MM_FAULT"] = fault
+        try:
+            op = mm.MegaMoE(cfg.E, cfg.P, cfg.k, cfg.H, cfg.I, debug=debug)
+        finally:
+            os.environ.pop("MM_FAULT", None)
+        op.set_weights(*[torch.from_numpy(a).to(dev) for a in gpu_util.weights(cfg)])
+        op.reserve(T)
+        op.set_route(mm.ROUTE_SMALL if route == 1 else mm.ROUTE_LARGE)
+        x = torch.from_numpy(hidden.view(np.int16)).to(dev).view(torch.bfloat16)
+        lg, b = torch.from_numpy(logits).to(dev), torch.from_numpy(bias).to(dev)
+        out = torch.empty_like(x)
+        op.forward(x, lg, b, out)
+        torch.cuda.synchronize()
+        assert op.get_status() == 0
+        outs.append(out.view(torch.int16).cpu().numpy().view(np.uint16))
+        op.close()
+    gpu_util.assert_out_close(outs[0], ref["out"])
+    assert np.array_equal(outs[0], outs[1])            # the checks change no result
