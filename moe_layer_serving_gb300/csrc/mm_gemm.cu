@@ -25,8 +25,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tv.row0 = g.tile_row0;
     tv.rows = g.tile_rows;
     tv.ntiles = *g.num_tiles;
-    tv.first = g.tile_first;
-    tv.experts = g.P;
     gemm_roles<Geo>(maps, g, tv, s, tmem);
     gemm_teardown(tmem);
 }
@@ -54,7 +52,6 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.tile_row0 = c->tile_row0;
     g.tile_rows = c->tile_rows;
     g.num_tiles = c->num_tiles;
-    g.tile_first = c->toff;
     g.done1 = c->done1;
     g.unit_next = c->unit_next;
     g.status = c->status;

@@ -90,29 +90,16 @@ struct Unit {
 };
 
 // Token tiles the GEMMs run over (generic pointers: global or shared memory).
-// first (optional): each expert's first tile, the tiles of an expert being
-// consecutive; with it the units of an expert are taken weight block by
-// weight block (see decode_unit).
 struct TileView {
     const int* expert;
     const int* row0;
     const int* rows;
     int ntiles;
-    const int* first;    // [experts] or null
-    int experts;
 };
 
-#ifndef MM_EXPERT_MAJOR
-#define MM_EXPERT_MAJOR 1
-#endif
-
-// Unit u -> (phase, tile, weight block).  Within a phase, the units of one
-// expert occupy the range [first * nb, (first + n) * nb) of its n tiles.
-// Inside that range they run block by block, the expert's tiles of one weight
-// block back to back, so that the SMs that take them read the same weight
-// block at about the same time and all but the first find it in L2 (taken
-// tile by tile, a hot expert's second tile re-read each block 16 (GEMM1) or 28
-// (GEMM2) units later, after the block had often left L2).
+// Unit u -> (phase, tile, weight block), tile by tile: the units of one tile
+// are consecutive, so the SMs that take them read that tile's token rows at
+// about the same time.
 __device__ __forceinline__ bool decode_unit(const GemmArgs& g, const TileView& tv, int u, Unit& un)
 {
     const int nb1 = g.I / kTile;
@@ -120,18 +107,14 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& g, const TileView& t
     const int units1 = (g.phases & 1) ? tv.ntiles * nb1 : 0;
     const int units2 = (g.phases & 2) ? tv.ntiles * nb2 : 0;
     if (u >= units1 + units2) return false;
-    const int nb = u < units1 ? nb1 : nb2;
-    const int uu = u < units1 ? u : u - units1;
-    un.phase = u < units1 ? 1 : 2;
-    un.tile = uu / nb;
-    un.blk = uu % nb;
-    if (MM_EXPERT_MAJOR && tv.first) {
-        const int p = tv.expert[un.tile];
-        const int f = tv.first[p];
-        const int n = (p + 1 < tv.experts ? tv.first[p + 1] : tv.ntiles) - f;
-        const int local = uu - f * nb;
-        un.blk = local / n;
-        un.tile = f + local % n;
+    if (u < units1) {
+        un.phase = 1;
+        un.tile = u / nb1;
+        un.blk = u % nb1;
+    } else {
+        un.phase = 2;
+        un.tile = (u - units1) / nb2;
+        un.blk = (u - units1) % nb2;
     }
     un.expert = tv.expert[un.tile];
     un.row0 = tv.row0[un.tile];

@@ -157,7 +157,6 @@ struct GemmArgs {
     const int* tile_row0;
     const int* tile_rows;
     const int* num_tiles;
-    const int* tile_first;  // per expert: its first token tile
     int* done1;             // per token tile: GEMM1 units finished
     int* unit_next;         // next unit to hand out (zeroed before the GEMM phase)
     int* status;

@@ -326,8 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tv.row0 = t_row0;
         tv.rows = t_rows;
         tv.ntiles = scal[0];
-        tv.first = nullptr;         // a few tiles per expert: tile by tile
-        tv.experts = P;
         if (short_tiles)
             gemm_roles<GeomSmall>(maps, g, tv, s, tmem);
         else
