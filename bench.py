@@ -358,6 +358,7 @@ def main():
     stream.synchronize()
     assert op.get_status() == 0
     route, launches, _ = op.last_info()
+    gemm_kind = op.last_gemm()
     phys = op.debug_dump(2)
     touched = int(np.unique(phys).size)
 
@@ -420,7 +421,7 @@ def main():
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         peaks = json.load(open(pk))
-    kname = "gemm16_kernel" if a16 else ("small_kernel" if route == 1 else "gemm_kernel")
+    kname = {0: "small_kernel", 1: "gemm_kernel", 2: "gemm2_kernel", 3: "gemm16_kernel"}[gemm_kind]
     wname = workload_config(cfg, args.act, args.route, args.shared)["workload"]
     if cfg.T <= 512:
         alg = touched * expert_bytes(cfg)           # weight streaming: the touched experts' bytes

@@ -213,9 +213,11 @@ MM_API mm_status mm_get_status(mm_handle h, int *device_code);
  * dst_host; MM_ERR_INVALID_ARG for an unknown stage. */
 MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t bytes);
 
-/* Stage 10 of mm_debug_dump: int32 [3] = {route taken by the last forward
+/* Stage 10 of mm_debug_dump: int32 [4] = {route taken by the last forward
  * (1 small, 2 large), number of kernels it launched, site of the last
- * device-side timeout (0 none; see WaitSite in the sources)}.
+ * device-side timeout or check (0 none; see WaitSite in the sources), the
+ * grouped GEMM kernel of the large path (0 none, 1 one CTA per unit, 2 CTA
+ * pairs with 2-SM MMAs, 3 the a16w4 kernel)}.
  * Stage 11: uint64 [SMs][8] %globaltimer readings (ns) of each CTA of the last
  * fused small-input launch at its stage boundaries: start, routed, past
  * barrier 1, dispatched, past barrier 2, GEMMs done, past barrier 3, end.

@@ -298,6 +298,11 @@ class MegaMoE:
         a = self.debug_dump(10)
         return int(a[0]), int(a[1]), int(a[2])
 
+    def last_gemm(self) -> int:
+        """Grouped GEMM kernel of the last forward: 0 none (fused small-input
+        kernel), 1 one CTA per unit, 2 CTA pairs (2-SM MMAs), 3 a16w4."""
+        return int(self.debug_dump(10)[3])
+
     def debug_dump(self, stage: int) -> np.ndarray:
         """Intermediate `stage` of the last forward as a flat array (see DUMP_STAGES)."""
         n = C.c_size_t(0)

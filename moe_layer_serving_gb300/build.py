@@ -16,7 +16,8 @@ LIB = os.path.join(HERE, "libmegamoe.so")
 # every indexed access of the SIMT stages and the GEMM tile decode is checked,
 # a failed check latches MM_ERR_DEVICE with its site and skips the access
 DEBUG_LIB = os.path.join(HERE, "libmegamoe_debug.so")
-SOURCES = ["mm_api.cu", "mm_route.cu", "mm_gemm.cu", "mm_gemm16.cu", "mm_small.cu", "mm_noalloc.cu", "mm_ep.cu"]
+SOURCES = ["mm_api.cu", "mm_route.cu", "mm_gemm.cu", "mm_gemm2.cu", "mm_gemm16.cu", "mm_small.cu", "mm_noalloc.cu",
+           "mm_ep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

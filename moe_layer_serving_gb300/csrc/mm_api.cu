@@ -50,6 +50,22 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t cols,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale tiles [n][512 bytes] read by TMA: rows of 256 bytes, a box of
+// `box_rows` rows (2 = one tile, 4 = a block pair's two tiles), no swizzle, so
+// shared memory receives the bytes as they are.
+bool make_sf_map(CUtensorMap* m, void* base, uint64_t ntiles, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {256, 2 * ntiles};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {256, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Weight blocks [nblocks][128 rows][128 e2m1]; a box is `depth` consecutive
 // blocks (a GEMM unit's pair, or one block).
 bool make_weight_map(CUtensorMap* m, void* base, uint64_t nblocks, uint32_t depth)
@@ -171,7 +187,9 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
     c->small_max = env_int("MM_SMALL_M_MAX", mm::kSmallMaxTokens);
     if (c->small_max > mm::kSmallMaxTokens) c->small_max = mm::kSmallMaxTokens;
     c->large_min = env_int("MM_LARGE_M_MIN", 1024);
-    if (mm::gemm_prepare(dev) != cudaSuccess || mm::small_prepare() != cudaSuccess ||
+    c->gemm_2sm = env_int("MM_GEMM_2SM", 0) != 0;
+    if (mm::gemm_prepare(dev) != cudaSuccess || mm::gemm2_prepare(dev) != cudaSuccess ||
+        mm::small_prepare() != cudaSuccess ||
         mm::gemm16_prepare() != cudaSuccess ||
         cudaMalloc(&c->counts, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
         cudaMemset(c->counts, 0, sizeof(int64_t) * MM_MAX_LAYERS * E) != cudaSuccess ||
@@ -249,7 +267,8 @@ mm_status mm_set_weights(mm_handle c, const uint8_t* w1, const uint8_t* w1s, con
     CK(mm::launch_tile_scales(w2s, c->w2_sf, static_cast<int64_t>(P * H), c->I, o2, nullptr));
     CK(cudaDeviceSynchronize());
     if (!make_weight_map(&c->maps.w1, c->w1, b1, 2) || !make_weight_map(&c->maps.w2, c->w2, b2, 2) ||
-        !make_weight_map(&c->maps.w2_one, c->w2, b2, 1))
+        !make_weight_map(&c->maps.w2_one, c->w2, b2, 1) || !make_weight_map(&c->maps.w1_one, c->w1, b1, 1) ||
+        !make_sf_map(&c->maps.w1_sf, c->w1_sf, b1, 4) || !make_sf_map(&c->maps.w2_sf, c->w2_sf, b2, 4))
         return MM_ERR_CUDA;
     c->maps_weights = true;
     c->weights_set = true;
@@ -469,7 +488,8 @@ mm_status mm::reserve_pairs(mm_handle c, int64_t npairs, int64_t max_tokens)
     add(chunks * P * 4);
     add((P + 1) * 4);
     add(P * 4);                               // first tile of each expert
-    add(tiles * 4 * 4 + 8);                   // tile table, done1, num_tiles, unit counter
+    add(tiles * 4 * 4 + 16);                  // tile table, done1, num_tiles, unit counter, pair count
+    add(tiles * 2 * 4);                       // tile pairs
     const int64_t eb = c->act == MM_ACT_BF16 ? 2 : 1;     // bytes per dispatched activation element
     add(rows * H * eb);
     add(tiles * (H / 128) * 512);
@@ -499,8 +519,9 @@ mm_status mm::reserve_pairs(mm_handle c, int64_t npairs, int64_t max_tokens)
     c->tile_row0 = carve<int32_t>(p, tiles);
     c->tile_rows = carve<int32_t>(p, tiles);
     c->done1 = carve<int32_t>(p, tiles);
-    c->num_tiles = carve<int32_t>(p, 2);
+    c->num_tiles = carve<int32_t>(p, 4);
     c->unit_next = c->num_tiles + 1;
+    c->st_tile = carve<int32_t>(p, tiles * 2);
     c->xq = carve<uint8_t>(p, rows * H * eb);
     c->xs_t = carve<uint8_t>(p, tiles * (H / 128) * 512);
     c->hq = carve<uint8_t>(p, rows * I * eb);
@@ -518,7 +539,9 @@ mm_status mm::reserve_pairs(mm_handle c, int64_t npairs, int64_t max_tokens)
                  make_map(&c->maps16.hb[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->hq, I, rows, I * 2, mm::kBBox << i,
                           64);
         else
-            ok = make_map(&c->maps.xq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox << i) &&
+            ok = make_sf_map(&c->maps.xs_sf, c->xs_t, tiles * (H / 128), 2) &&
+                 make_sf_map(&c->maps.hs_sf, c->hs_t, tiles * (I / 128), 2) &&
+                 make_map(&c->maps.xq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->xq, H, rows, H, mm::kBBox << i) &&
                  make_map(&c->maps.hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, c->hq, I, rows, I, mm::kBBox << i);
         if (!ok) {
             free_ws(c);
@@ -562,6 +585,7 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
         if (prof16) ++c->prof_used;
         c->last_route = 2;
         c->last_launches = 7;
+        c->last_gemm = 3;
         c->last_T = T;
         c->last_stream = s;
         return MM_OK;
@@ -586,6 +610,7 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     if (prof) ++c->prof_used;
     c->last_route = small ? 1 : 2;
     c->last_launches = small ? 1 : 7;
+    c->last_gemm = small ? 0 : (mm::gemm2_usable(c) ? 2 : 1);
     c->last_T = T;
     c->last_stream = s;
     return MM_OK;
@@ -672,7 +697,7 @@ static mm_status debug_geometry(mm_handle c, int stage, size_t* bytes, int32_t* 
         case 7: *bytes = static_cast<size_t>(rows) * c->I * (a16 ? 2 : 1); break;
         case 8: *bytes = a16 ? 0 : static_cast<size_t>(rows) * c->I / 32; break;
         case 9: *bytes = static_cast<size_t>(rows) * c->H * 2; break;
-        case 10: *bytes = 3 * sizeof(int32_t); break;
+        case 10: *bytes = 4 * sizeof(int32_t); break;
         case 11: *bytes = static_cast<size_t>(c->sms) * 8 * sizeof(uint64_t); break;
         case 12: {
             int32_t ntiles = 0;
@@ -704,7 +729,7 @@ mm_status mm_debug_dump(mm_handle c, int stage, void* dst, size_t bytes)
     if (stage == 10) {
         int32_t site = 0;
         CK(cudaMemcpy(&site, c->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost));
-        const int32_t info[3] = {c->last_route, c->last_launches, site ? site : c->last_site};
+        const int32_t info[4] = {c->last_route, c->last_launches, site ? site : c->last_site, c->last_gemm};
         memcpy(dst, info, n);
         return MM_OK;
     }

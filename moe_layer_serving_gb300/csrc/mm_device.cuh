@@ -144,6 +144,94 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// thread-block clusters: rank, peer shared memory, cluster-wide barrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// arrive (release at cluster scope) on an mbarrier of another CTA of the cluster
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// try_wait with acquire at cluster scope (for arrivals made by another CTA)
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait as mbar_wait, with acquire at cluster scope.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status, volatile int* abort,
+                                                  int site)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort) return false;
+        if (globaltimer() - t0 > kPipeWaitLimitNs) {
+            latch_error(status, MM_ERR_TIMEOUT, site);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// every thread of every CTA of the cluster
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Tile loads into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, int32_t x, int32_t y, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Ask for global bytes to be brought into L2 (no completion, no destination).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes)
 {
@@ -247,6 +335,65 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
                  : "memory");
 }
 
+// ---- the 2-SM forms (cta_group::2): a CTA pair of a cluster works as one
+// MMA.  Tensor memory is allocated collectively (one warp in each CTA, the
+// same columns in both); the even CTA issues the MMAs, which take A's M rows
+// half from each CTA's shared memory (its 128 rows of D in its own tensor
+// memory) and B's N rows half from each; the block scales of A are each CTA's
+// own rows', those of B cover all N in both CTAs' tensor memory; a scale copy
+// issued by the even CTA moves each CTA's shared memory into its own tensor
+// memory.  A kernel uses only one cta_group.
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish2()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+template <bool kAccumulate>
+__device__ __forceinline__ void mma2_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem)
+{
+    if (kAccumulate)
+        asm volatile(
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 1;" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 0;" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+}
+
+// arrive on the mbarrier at this offset in each CTA of cta_mask once the
+// pair's prior tcgen05 operations have completed
+__device__ __forceinline__ void tc_commit2_mc(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_cp2_32x128b_x4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 32 rows x 128 bits of shared memory into tensor memory, replicated into all
 // four 32-lane quarters (the scale-factor layout the block-scaled MMA reads).
 __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
@@ -295,7 +442,7 @@ __device__ __forceinline__ uint64_t desc_sf(const void* sf)
 // Instruction descriptor, block-scaled kinds: A = e4m3 (format 0), B = e2m1
 // (format 5), e8m0 scales, both K-major, M = 128, N = n (multiple of 16, <= 256);
 // sf_id picks the scale byte (the 32-wide K block) inside each scale column.
-__device__ __forceinline__ uint32_t idesc_e4m3_e2m1(uint32_t n, uint32_t sf_id)
+__device__ __forceinline__ uint32_t idesc_e4m3_e2m1(uint32_t n, uint32_t sf_id, uint32_t m = 128)
 {
     uint32_t d = 0;
     d |= (sf_id & 3u) << 4;       // B scale-factor byte
@@ -303,7 +450,7 @@ __device__ __forceinline__ uint32_t idesc_e4m3_e2m1(uint32_t n, uint32_t sf_id)
     d |= 5u << 10;                // B format: e2m1
     d |= (n >> 3) << 17;          // N / 8
     d |= 1u << 23;                // scale format: ue8m0
-    d |= (128u >> 4) << 24;       // M / 16
+    d |= (m >> 4) << 24;          // M / 16 (256 for a CTA pair)
     d |= (sf_id & 3u) << 29;      // A scale-factor byte
     return d;
 }

@@ -61,11 +61,13 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.phases = 3;
     g.fault = c->fault;
     g.rows_cap = static_cast<int>(c->rows_cap);
+    g.st_tile = c->st_tile;
 }
 
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)
 {
     (void)T;
+    if (gemm2_usable(c)) return launch_gemm2(c, s);
     GemmArgs g;
     fill_gemm_args(c, &g);
     cudaLaunchConfig_t cfg = {};

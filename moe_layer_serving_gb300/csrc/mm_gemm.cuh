@@ -60,6 +60,8 @@ constexpr uint32_t kColSF = 256, kSFSlotCols = 16, kColSFB = 4;
 // ignores.  The fused small-input kernel uses short tiles so that one more
 // stage fits: with few tokens per expert its time is the weight stream's,
 // set by how many bytes each SM keeps in flight.
+constexpr int kBarBlock = 512;           // bytes of mbarriers and scalars after the stages
+
 template <int kRows_, int kStages_>
 struct Geom {
     static constexpr int kRows = kRows_;
@@ -67,7 +69,7 @@ struct Geom {
     static constexpr int kABytes = kRows * kKStep;
     static constexpr int kStageBytes = kABytes + 2 * kWBoxBytes + 4 * kSFBytes;
     static constexpr int kStageRegion = kStages * kStageBytes;
-    static constexpr int kSmemBytes = kStageRegion + 256;   // stages + barriers
+    static constexpr int kSmemBytes = kStageRegion + kBarBlock;   // stages + barriers
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert(kRows % 16 == 0 && kRows <= 128, "token rows per stage");
     static_assert(kStages <= 8, "barrier block holds eight stages");
@@ -160,13 +162,22 @@ struct GemmSmem {
     uint64_t* ufull;          // [kURing] unit slot written (producer)
     uint64_t* uempty;         // [kURing] unit slot read (MMA thread + every epilogue thread)
     uint64_t* drain;          // the MMA thread's own wait for its issued work after an abort
+    // CTA pairs (the 2-SM GEMM): the unit numbers CTA 0 draws reach CTA 1
+    // through CTA 1's inbox; CTA 1 reports its drained accumulator to CTA 0,
+    // which issues the pair's MMAs
+    uint64_t* inbox_full;     // [kURing] in CTA 1: a number arrived
+    uint64_t* inbox_free;     // [kURing] in CTA 0: CTA 1 took a number out
+    uint64_t* peer_tmem_empty;  // in CTA 0: CTA 1's epilogue drained its accumulator
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     volatile int* uring;      // [kURing] unit numbers
+    volatile int* inbox;      // [kURing] numbers drawn by CTA 0 (in CTA 1)
 };
-// Barrier block (256 bytes): full[8], empty[8], tmem_full, tmem_empty,
-// ufull[4], uempty[4], drain, the TMEM base, the abort flag and the unit ring.  Its layout does not depend on the stage
-// count, so one kernel can run either geometry over the same buffers.
+// Barrier block (kBarBlock bytes): full[8], empty[8], tmem_full, tmem_empty,
+// ufull[4], uempty[4], drain, inbox_full[4], inbox_free[4],
+// peer_tmem_empty, then the TMEM base, the abort flag, the unit ring and the
+// inbox.  Its layout does not depend on the stage count, so one kernel can run
+// either geometry over the same buffers.
 constexpr int kMaxStages = 8;
 __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
 {
@@ -179,10 +190,14 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
     s.ufull = s.tmem_empty + 1;
     s.uempty = s.ufull + kURing;
     s.drain = s.uempty + kURing;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.inbox_full = s.drain + 1;
+    s.inbox_free = s.inbox_full + kURing;
+    s.peer_tmem_empty = s.inbox_free + kURing;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.peer_tmem_empty + 1);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
     s.uring = s.abort_flag + 1;
-    static_assert((2 * kMaxStages + 3 + 2 * kURing) * 8 + 8 + 4 * kURing <= 256, "barrier block");
+    s.inbox = s.uring + kURing;
+    static_assert((2 * kMaxStages + 4 + 4 * kURing) * 8 + 8 + 8 * kURing <= kBarBlock, "barrier block");
     return s;
 }
 
@@ -243,10 +258,37 @@ struct UnitQueue {
     }
 };
 
-// Producer: take the next unit number and queue it for the CTA's consumers.
-__device__ __forceinline__ bool push_unit(const GemmArgs& g, const GemmSmem& s, UnitQueue& q, int& u)
+// CTA pairs: CTA 0 draws the next number and hands it to CTA 1 through CTA
+// 1's inbox (a remote store and a remote arrive); CTA 1 takes it out and
+// frees the slot with a remote arrive on CTA 0's inbox_free.  Bounded waits.
+__device__ __forceinline__ bool pair_draw(const GemmArgs& g, const GemmSmem& s, UnitQueue& box, uint32_t rank, int& u)
 {
-    u = *s.abort_flag ? 0x7FFFFFFF : atomicAdd(g.unit_next, 1);
+    if (rank == 0) {
+        u = *s.abort_flag ? 0x7FFFFFFF : atomicAdd(g.unit_next, 1);
+        if (!mbar_wait_cluster(&s.inbox_free[box.slot], box.phase ^ 1u, g.status, s.abort_flag, kSiteUnitQueue))
+            return false;
+        st_peer_u32(peer_addr(const_cast<int*>(&s.inbox[box.slot]), 1), static_cast<uint32_t>(u));
+        mbar_arrive_peer(peer_addr(&s.inbox_full[box.slot], 1));
+    } else {
+        if (!mbar_wait_cluster(&s.inbox_full[box.slot], box.phase, g.status, s.abort_flag, kSiteUnitQueue))
+            return false;
+        u = s.inbox[box.slot];
+        mbar_arrive_peer(peer_addr(&s.inbox_free[box.slot], 0));
+    }
+    box.advance();
+    return true;
+}
+
+// Producer: take the next unit number (drawn here, or for the second CTA of a
+// pair handed over by the first) and queue it for the CTA's consumers.
+__device__ __forceinline__ bool push_unit(const GemmArgs& g, const GemmSmem& s, UnitQueue& q, int& u,
+                                          UnitQueue* box = nullptr, uint32_t rank = 0)
+{
+    if (box) {
+        if (!pair_draw(g, s, *box, rank, u)) return false;
+    } else {
+        u = *s.abort_flag ? 0x7FFFFFFF : atomicAdd(g.unit_next, 1);
+    }
     if (!mbar_wait(&s.uempty[q.slot], q.phase ^ 1u, g.status, s.abort_flag, kSiteUnitQueue)) return false;
     s.uring[q.slot] = u;
     mbar_arrive(&s.ufull[q.slot]);
@@ -454,8 +496,11 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16])
 // ---- epilogue: warps 2..9 ------------------------------------------------------
 // Warp w reads TMEM lanes 32*(w % 4) .. +32 (token rows) and column half
 // (w - 2) / 4 of the unit's columns.
-__device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView& tv, const GemmSmem& s,
-                                              uint32_t tmem)
+// dec(u, un): the unit behind number u (false: none).  A unit whose tile is
+// absent (rows 0: the second CTA of a pair whose expert had an odd number of
+// tiles) is drained and released like any other, and writes nothing.
+template <class Dec>
+__device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem& s, uint32_t tmem, const Dec& dec)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;                       // TMEM lane quarter
@@ -467,7 +512,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView&
     UnitQueue uq;
     for (;;) {
         int u;
-        if (!pop_unit(g, s, uq, u) || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
+        if (!pop_unit(g, s, uq, u) || *s.abort_flag || !dec(u, un)) break;
         if (!mbar_wait(s.tmem_full, acc_phase, g.status, s.abort_flag, kSiteEpiTmemFull)) break;
         tc_fence_after();
         const bool active = 32 * q < un.rows;                       // warp-uniform
@@ -526,7 +571,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const TileView&
             fence_proxy_async_global();
             __threadfence();
             epi_bar_sync();
-            if (threadIdx.x == kEpiWarp0 * 32) atomicAdd(&g.done1[un.tile], 1);
+            if (threadIdx.x == kEpiWarp0 * 32 && un.rows > 0) atomicAdd(&g.done1[un.tile], 1);
         } else {
             // columns [half*128, +128) of this unit's weight rows
             const bool cols = half < un.nw;
@@ -572,7 +617,7 @@ __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs&
     } else if (warp == 1) {
         mma_loop<G>(g, tv, s, tmem);
     } else {
-        epilogue_loop(g, tv, s, tmem);
+        epilogue_loop(g, s, tmem, [&](int u, Unit& un) { return decode_unit(g, tv, u, un); });
     }
 }
 

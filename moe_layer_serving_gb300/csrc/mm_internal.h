@@ -113,7 +113,10 @@ constexpr int kTokBoxes = 4;     // token-operand maps with boxes of 16, 32, 64,
 struct GemmMaps {
     CUtensorMap w1;            // W1 blocks, box = the unit's block pair (z extent 2)
     CUtensorMap w2;            // W2 blocks, box = block pair
-    CUtensorMap w2_one;        // W2 blocks, box = one block (ragged last group)
+    CUtensorMap w2_one;        // W2 blocks, box = one block (ragged last group; each CTA of a pair)
+    CUtensorMap w1_one;        // W1 blocks, box = one block (each CTA of a pair)
+    CUtensorMap w1_sf, w2_sf;  // weight scale tiles as rows of 256 bytes, box = a block pair's two tiles
+    CUtensorMap xs_sf, hs_sf;  // token-tile scale tiles, box = one tile
     CUtensorMap xq[kTokBoxes]; // e4m3 [rows][H], box 16 << i rows
     CUtensorMap hq[kTokBoxes]; // e4m3 [rows][I], box 16 << i rows
 };
@@ -164,6 +167,7 @@ struct GemmArgs {
     int phases;             // bit 0: GEMM1 units, bit 1: GEMM2 units
     int fault;              // injected fault (FaultSite), 0 = none
     int rows_cap;           // dispatch rows reserved (bounds checks of debug builds)
+    const int* st_tile;     // the 2-SM GEMM's tile pairs [2 * num_tiles[2]]
 };
 
 }  // namespace mm
@@ -175,6 +179,7 @@ struct mm_ctx {
     int small_max = 512, large_min = 1024;
     int route = MM_ROUTE_AUTO, layer = 0, recording = 0;
     int fault = 0;                  // mm::FaultSite
+    bool gemm_2sm = false;          // large-input GEMM on CTA pairs when the shapes allow (MM_GEMM_2SM=1)
     // weights (library-owned)
     uint8_t *w1 = nullptr, *w1_sf = nullptr, *w2 = nullptr, *w2_sf = nullptr;
     bool weights_set = false;
@@ -194,6 +199,7 @@ struct mm_ctx {
     int32_t *chunk_hist = nullptr, *off = nullptr, *toff = nullptr, *tile_expert = nullptr, *tile_row0 = nullptr,
             *tile_rows = nullptr, *num_tiles = nullptr, *done1 = nullptr;
     int32_t* unit_next = nullptr;   // the GEMM kernels' unit counter (num_tiles[1])
+    int32_t* st_tile = nullptr;     // tile pairs of the 2-SM GEMM [2 * tiles] (count in num_tiles[2])
     uint8_t *xq = nullptr, *xs_t = nullptr, *hq = nullptr, *hs_t = nullptr;
     __nv_bfloat16* y = nullptr;
     int* status = nullptr;
@@ -220,6 +226,7 @@ struct mm_ctx {
     int64_t ep_send_rows = 0;          // send-buffer rows of the last mm_ep_dispatch
     // last forward (debug dumps)
     int last_route = 0, last_launches = 0, last_site = 0;
+    int last_gemm = 0;              // grouped GEMM kernel of the last forward (stage 10 of mm_debug_dump)
     int64_t last_T = 0;
     cudaStream_t last_stream = nullptr;
 };
@@ -279,6 +286,9 @@ cudaError_t launch_combine(const mm_ctx* c, void* out, int64_t T, cudaStream_t s
 cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
 cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
 cudaError_t gemm_prepare(int dev);
+cudaError_t gemm2_prepare(int dev);
+bool gemm2_usable(const mm_ctx* c);        // the large-input GEMM runs on CTA pairs for this handle
+cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s);
 cudaError_t gemm16_prepare();
 cudaError_t launch_gemm16(const mm_ctx* c, cudaStream_t s);
 cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);

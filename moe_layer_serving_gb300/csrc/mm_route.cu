@@ -93,8 +93,9 @@ struct ScanArgs {
     int32_t* tile_expert;
     int32_t* tile_row0;
     int32_t* tile_rows;
-    int32_t* num_tiles;    // [0] tiles; [1] the GEMM kernel's unit counter, reset here
+    int32_t* num_tiles;    // [0] tiles; [1] the GEMM kernel's unit counter, reset here; [2] tile pairs
     int32_t* done1;
+    int32_t* st_tile;      // [2 * pairs]: the two tiles of each pair of an expert's tiles (second -1 if none)
 };
 
 __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
@@ -121,11 +122,14 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
     }
     const int padded = seg_rows(cnt);
     const int tiles = tiles_of(cnt);
+    const int pairs = (tiles + 1) / 2;
     const int off_incl = block_scan_incl(padded, warp_tot);
     const int tiles_incl = block_scan_incl(tiles, warp_tot);
+    const int pairs_incl = block_scan_incl(pairs, warp_tot);
     if (p < a.P) {
         const int off = off_incl - padded;
         const int t0 = tiles_incl - tiles;
+        const int s0 = pairs_incl - pairs;
         a.off[p] = off;
         a.toff[p] = t0;
         for (int t = 0; t < tiles; ++t) {
@@ -134,10 +138,16 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
             a.tile_rows[t0 + t] = min(kTokTile, cnt - t * kTokTile);
             a.done1[t0 + t] = 0;
         }
+        // the expert's tiles two by two, for the GEMM on CTA pairs
+        for (int i = 0; i < pairs; ++i) {
+            a.st_tile[2 * (s0 + i)] = t0 + 2 * i;
+            a.st_tile[2 * (s0 + i) + 1] = 2 * i + 1 < tiles ? t0 + 2 * i + 1 : -1;
+        }
         if (p == a.P - 1) {
             a.off[a.P] = off_incl;
             a.num_tiles[0] = tiles_incl;
             a.num_tiles[1] = 0;
+            a.num_tiles[2] = pairs_incl;
         }
     }
 }
@@ -331,6 +341,7 @@ cudaError_t launch_permute_ids(const mm_ctx* c, const int32_t* ids, int64_t npai
     a.tile_rows = c->tile_rows;
     a.num_tiles = c->num_tiles;
     a.done1 = c->done1;
+    a.st_tile = c->st_tile;
     scan_kernel<<<1, 512, 0, s>>>(a);
     scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(ids, npairs, P, c->chunk_hist, c->off, pos);
     return cudaGetLastError();

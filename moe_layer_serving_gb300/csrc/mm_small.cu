@@ -37,7 +37,7 @@ constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
 constexpr int kStageRegion =
     GeomSmall::kStageRegion > GeomLarge::kStageRegion ? GeomSmall::kStageRegion : GeomLarge::kStageRegion;
 constexpr int kMaxSmallTiles = MM_MAX_EXPERTS + kMaxSmallPairs / kSmallTile + 1;
-constexpr int kSmallSmemBytes = kStageRegion + 256 + 3 * kMaxSmallTiles * 4 + 64 + 1024;
+constexpr int kSmallSmemBytes = kStageRegion + kBarBlock + 3 * kMaxSmallTiles * 4 + 64 + 1024;
 static_assert(kSmallSmemBytes <= 232448, "shared memory per block");
 
 struct SmallArgs {
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const GemmSmem s = gemm_smem(smem, smem + kStageRegion);
-    int* t_expert = reinterpret_cast<int*>(smem + kStageRegion + 256);
+    int* t_expert = reinterpret_cast<int*>(smem + kStageRegion + kBarBlock);
     int* t_row0 = t_expert + kMaxSmallTiles;
     int* t_rows = t_row0 + kMaxSmallTiles;
     int* scal = t_rows + kMaxSmallTiles;            // [0] tiles, [1] rows, [2] [3] tile counts

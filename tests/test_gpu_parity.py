@@ -238,3 +238,39 @@ def test_fused_shared_expert_decode_shapes():
     run.close()
     assert res["status"] == 0
     gpu_util.check_against_oracle(cfg, res, hidden, logits, bias, W, None, gpu_util.sample_tokens(cfg.T, 16), shared=1)
+
+
+@pytest.mark.parametrize("H,I,T,E,k", [(512, 256, 1500, 12, 4), (512, 512, 1100, 8, 2), (768, 256, 600, 16, 3),
+                                       (384, 256, 1100, 8, 2)])
+def test_two_sm_gemm_matches_one_cta_gemm(H, I, T, E, k):
+    # The large-input GEMM runs on CTA pairs (one 2-SM MMA over two token
+    # tiles of an expert) when H is a multiple of 256; MM_GEMM_2SM=0 runs the
+    # one-CTA kernel.  Experts with an odd number of tiles leave the second
+    # CTA of their last pair without a tile.  Both kernels must give identical
+    # intermediates and outputs (each row's MMAs and epilogue are the same),
+    # and match the oracle.  H = 384 takes the one-CTA kernel either way.
+    import dataclasses
+    import os
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T, H=H, I=I, E=E, P=E, k=k)
+    hidden, logits, bias = synthetic.make_activations(cfg)
+    logits[:, 0] += 3.0                 # one hot expert: many tiles
+    W = synthetic.make_all_weights(cfg)
+    res = {}
+    for two_sm in ("1", "0"):
+        os.environ["MM_GEMM_2SM"] = two_sm
+        try:
+            run = gpu_util.Run(cfg, W, cap=cfg.T)
+        finally:
+            del os.environ["MM_GEMM_2SM"]
+        run.op.set_route(2)
+        res[two_sm] = run.forward(hidden, logits, bias)
+        run.close()
+        assert res[two_sm]["status"] == 0
+    tiles = res["1"]["tiles"].reshape(-1, 3)
+    per_expert = np.bincount(tiles[:, 0], minlength=cfg.P)
+    assert (per_expert >= 2).any()
+    if T != 1500:
+        assert (per_expert % 2 == 1).any()          # an expert with an odd number of tiles
+    for name in ("hq", "hs", "y", "out"):
+        assert np.array_equal(res["1"][name], res["0"][name]), name
+    gpu_util.check_against_oracle(cfg, res["1"], hidden, logits, bias, W, None, gpu_util.tile_edge_tokens(res["1"], T))
