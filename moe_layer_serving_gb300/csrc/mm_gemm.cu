@@ -62,6 +62,7 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.fault = c->fault;
     g.rows_cap = static_cast<int>(c->rows_cap);
     g.st_tile = c->st_tile;
+    g.keep_weights = 0;
 }
 
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)
@@ -70,6 +71,11 @@ cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)
     if (gemm2_usable(c)) return launch_gemm2(c, s);
     GemmArgs g;
     fill_gemm_args(c, &g);
+    // Large batches give an expert several token tiles, each re-reading the
+    // expert's weight blocks: loading them with the normal L2 policy rather
+    // than evict-first measured 2% faster on the skewed 16384-token layer (its
+    // hot experts have tens of tiles) and the same on uniform prefill.
+    g.keep_weights = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c->sms));
     cfg.blockDim = dim3(kThreads);

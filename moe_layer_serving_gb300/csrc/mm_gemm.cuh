@@ -311,7 +311,7 @@ template <class G>
 __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                               const GemmSmem& s)
 {
-    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_w = g.keep_weights ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;

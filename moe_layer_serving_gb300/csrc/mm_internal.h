@@ -168,6 +168,8 @@ struct GemmArgs {
     int fault;              // injected fault (FaultSite), 0 = none
     int rows_cap;           // dispatch rows reserved (bounds checks of debug builds)
     const int* st_tile;     // the 2-SM GEMM's tile pairs [2 * num_tiles[2]]
+    int keep_weights;       // 1: weight loads with the normal L2 policy (an expert's tiles re-read its
+                            // weights); 0: evict-first (streamed once, the fused small-input kernel)
 };
 
 }  // namespace mm
