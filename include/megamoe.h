@@ -322,8 +322,10 @@ MM_API mm_status mm_ep_reserve(mm_handle h, int64_t max_tokens, int64_t max_recv
 MM_API mm_status mm_ep_send_rows(mm_handle h, int64_t num_tokens, int64_t *rows);
 
 /* Step 1, on the source rank.  hidden [T, H] bf16, logits [T, E] fp32 and
- * bias [E] fp32 (or NULL) as in mm_forward.  Writes, for rows = the value of
- * mm_ep_send_rows (caller-owned device buffers, 16-byte aligned):
+ * bias [E] fp32 (or NULL) as in mm_forward.  The send buffers are caller-owned
+ * device buffers of send_capacity rows each (16-byte aligned); they need the
+ * rows of mm_ep_send_rows(T), else MM_ERR_CAPACITY and nothing is enqueued.
+ * Writes, for rows = mm_ep_send_rows(T):
  *   send_xq  [rows, H]     e4m3 codes of each (token, slot) pair
  *   send_xs  [rows, H/32]  their e8m0 scales, row-major
  *   send_eid [rows] int32  the pair's expert index among its destination
@@ -336,7 +338,7 @@ MM_API mm_status mm_ep_send_rows(mm_handle h, int64_t num_tokens, int64_t *rows)
  * T > reserved tokens -> MM_ERR_CAPACITY; T == 0 -> all row_off 0. */
 MM_API mm_status mm_ep_dispatch(mm_handle h, const void *hidden, const float *logits, const float *bias,
                                 int64_t num_tokens, void *send_xq, void *send_xs, int32_t *send_eid,
-                                int64_t *row_off, mm_stream stream);
+                                int64_t send_capacity, int64_t *row_off, mm_stream stream);
 
 /* Step 2, on the destination rank.  recv_xq [n, H], recv_xs [n, H/32] and
  * recv_eid [n] are the rows this rank received (in any order of sources;

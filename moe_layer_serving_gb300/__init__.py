@@ -60,7 +60,7 @@ _SIGS = {
     "mm_set_expert_parallel": [_p, _i32, _i32, _p],
     "mm_ep_reserve": [_p, _i64, _i64],
     "mm_ep_send_rows": [_p, _i64, C.POINTER(_i64)],
-    "mm_ep_dispatch": [_p, _p, _p, _p, _i64, _p, _p, _p, _p, _p],
+    "mm_ep_dispatch": [_p, _p, _p, _p, _i64, _p, _p, _p, _i64, _p, _p],
     "mm_ep_experts": [_p, _p, _p, _p, _i64, _p, _p],
     "mm_ep_combine": [_p, _p, _p, _p],
 }
@@ -238,8 +238,13 @@ class MegaMoE:
         row offsets per destination rank, int64 [world + 1] (mm_ep_dispatch, synchronous)."""
         T = hidden.shape[0] if num_tokens is None else num_tokens
         off = np.zeros(self.ep_world + 1, np.int64)
+        cap = 0 if send_eid is None else int(send_eid.shape[0])
+        if send_xq is not None:
+            cap = min(cap, int(send_xq.shape[0]))
+        if send_xs is not None:
+            cap = min(cap, int(send_xs.shape[0]))
         _check(self._lib.mm_ep_dispatch(self._h, _addr(hidden), _addr(logits), _addr(bias), T, _addr(send_xq),
-                                        _addr(send_xs), _addr(send_eid), off.ctypes.data, _stream(stream)),
+                                        _addr(send_xs), _addr(send_eid), cap, off.ctypes.data, _stream(stream)),
                "mm_ep_dispatch")
         return off
 

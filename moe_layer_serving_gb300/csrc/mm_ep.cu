@@ -238,9 +238,10 @@ mm_status mm_ep_send_rows(mm_handle c, int64_t num_tokens, int64_t* rows)
 }
 
 mm_status mm_ep_dispatch(mm_handle c, const void* hidden, const float* logits, const float* bias, int64_t T,
-                         void* send_xq, void* send_xs, int32_t* send_eid, int64_t* row_off, mm_stream stream)
+                         void* send_xq, void* send_xs, int32_t* send_eid, int64_t send_capacity, int64_t* row_off,
+                         mm_stream stream)
 {
-    if (!c || T < 0 || !row_off) return MM_ERR_INVALID_ARG;
+    if (!c || T < 0 || !row_off || send_capacity < 0) return MM_ERR_INVALID_ARG;
     if (!c->ep) return MM_ERR_NOT_READY;
     if (!c->map_set) return MM_ERR_NOT_READY;
     if (T > c->cap_tokens) return MM_ERR_CAPACITY;
@@ -257,6 +258,7 @@ mm_status mm_ep_dispatch(mm_handle c, const void* hidden, const float* logits, c
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (mm::on_capture(s)) return MM_ERR_INVALID_ARG;          // reads the split sizes back to the host
     const int64_t rows = mm::send_rows(c, T);
+    if (rows > send_capacity) return MM_ERR_CAPACITY;
     if (cudaMemsetAsync(send_eid, 0xFF, sizeof(int32_t) * rows, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_route(c, logits, bias, T, s) != cudaSuccess) return MM_ERR_CUDA;
     if (mm::launch_permute(c, T, s) != cudaSuccess) return MM_ERR_CUDA;

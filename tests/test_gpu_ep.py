@@ -184,6 +184,17 @@ def test_expert_parallel_rank_with_no_rows_and_idle_batches(torch):
                          None, num_tokens=0)
     assert list(off) == [0, 0, 0]
     assert op.ep_send_rows(0) == 0
+    # send buffers smaller than mm_ep_send_rows: refused before anything is enqueued
+    dev = torch.device("cuda:0")
+    x = torch.zeros((16, cfg.H), dtype=torch.bfloat16, device=dev)
+    lg = torch.zeros((16, cfg.E), dtype=torch.float32, device=dev)
+    short = op.ep_send_rows(16) - 1
+    sxq = torch.empty((short, cfg.H), dtype=torch.uint8, device=dev)
+    sxs = torch.empty((short, cfg.H // 32), dtype=torch.uint8, device=dev)
+    seid = torch.empty((short,), dtype=torch.int32, device=dev)
+    with pytest.raises(mm.MegaMoEError) as err:
+        op.ep_dispatch(x, lg, None, sxq, sxs, seid)
+    assert err.value.status == mm.MM_ERR_CAPACITY
     # the single-GPU calls are refused on an expert-parallel handle
     assert mm.lib().mm_forward(op.handle, None, None, None, None, 1, None) == mm.MM_ERR_UNSUPPORTED
     assert mm.lib().mm_set_shared_experts(op.handle, 1) == mm.MM_ERR_UNSUPPORTED
