@@ -173,6 +173,14 @@ __device__ __forceinline__ void mbar_arrive_peer(uint32_t addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
+// Relaxed: orders nothing before it.  For signals whose only precondition is
+// already complete in the signalling thread (a tensor-memory read followed by
+// tcgen05.wait::ld); the release form measured ~1,000 cycles a call here.
+__device__ __forceinline__ void mbar_arrive_peer_relaxed(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
 // try_wait with acquire at cluster scope (for arrivals made by another CTA)
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
 {

@@ -27,7 +27,16 @@
 // behind).  All GEMM1 units precede all GEMM2 units, and a GEMM2 unit waits
 // (bounded) until the GEMM1 units of its tile have published hq.  Warp roles:
 // 0 = TMA producer (one lane), 1 = tensor-memory owner + MMA issuer (the whole
-// warp, one elected lane issuing), 2..9 = epilogue.  The eight epilogue warps
+// warp, one elected lane issuing), 2..9 = epilogue.
+//
+// Issuing a stage's copies takes one thread about 500 cycles (each bulk copy
+// ~130, each tensor copy ~60, the expect-tx arrive and the L2 prefetch more),
+// about as long as the stage's MMAs (555 cycles), so a single producer thread
+// cannot get ahead of the tensor cores again after a late stage.  The
+// large-input kernels therefore split the producer: warp 0 issues the token
+// side (token rows and their scales) and draws the units, warp 10 the weight
+// side (weight blocks, their scales, the L2 prefetch); each arrives on the
+// stage's full barrier with its own byte count.  The eight epilogue warps
 // first drain the accumulator into registers (each warp: its 32 token rows,
 // half of the columns) and release tensor memory, so the next unit's MMAs run
 // while they compute.
@@ -44,6 +53,8 @@
 namespace mm {
 
 constexpr int kThreads = 320;              // 10 warps
+constexpr int kWProdWarp = 10;             // the weight-side producer of a split kernel
+constexpr int kThreadsSplit = kThreads + 32;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -160,7 +171,7 @@ struct GemmSmem {
     uint64_t* tmem_full;
     uint64_t* tmem_empty;
     uint64_t* ufull;          // [kURing] unit slot written (producer)
-    uint64_t* uempty;         // [kURing] unit slot read (MMA thread + every epilogue thread)
+    uint64_t* uempty;         // [kURing] unit slot read (MMA warp, weight-side producer, every epilogue thread)
     uint64_t* drain;          // the MMA thread's own wait for its issued work after an abort
     // CTA pairs (the 2-SM GEMM): the unit numbers CTA 0 draws reach CTA 1
     // through CTA 1's inbox; CTA 1 reports its drained accumulator to CTA 0,
@@ -202,13 +213,16 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
 }
 
 // All threads: barriers, tensor-memory allocation (warp 1); returns the TMEM base.
-template <class G>
+// kSplit: two producer threads (token side and weight side) arrive on every
+// full barrier and take every unit out of the ring.
+template <class G, bool kSplit = false>
 __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps& maps)
 {
     const int warp = threadIdx.x >> 5;
+    constexpr uint32_t kProducers = kSplit ? 2 : 1;
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::kStages; ++i) {
-            mbar_init(&s.full[i], 1);
+            mbar_init(&s.full[i], kProducers);
             mbar_init(&s.empty[i], 1);
         }
         mbar_init(s.tmem_full, 1);
@@ -216,7 +230,7 @@ __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps
         mbar_init(s.drain, 1);
         for (int i = 0; i < kURing; ++i) {
             mbar_init(&s.ufull[i], 1);
-            mbar_init(&s.uempty[i], 1 + kEpiThreads);
+            mbar_init(&s.uempty[i], kProducers + kEpiThreads);
         }
         *s.abort_flag = 0;
         fence_mbar_init();
@@ -306,11 +320,17 @@ __device__ __forceinline__ bool pop_unit(const GemmArgs& g, const GemmSmem& s, U
     return true;
 }
 
-// ---- producer: one thread issues every TMA / bulk copy -----------------------
-template <class G>
+// ---- producer -----------------------------------------------------------------
+// kSide 0: one thread issues every copy; 1: the token side (draws the units,
+// waits for GEMM1 results before a GEMM2 unit); 2: the weight side (takes the
+// units out of the ring like the consumers).
+constexpr int kSideBoth = 0, kSideTokens = 1, kSideWeights = 2;
+
+template <class G, int kSide = kSideBoth>
 __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                               const GemmSmem& s)
 {
+    constexpr bool kTok = kSide != kSideWeights, kW = kSide != kSideTokens;
     const uint64_t pol_w = g.keep_weights ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
@@ -322,12 +342,13 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
     UnitQueue q;
     for (;;) {
         int u;
-        if (!push_unit(g, s, q, u) || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
+        const bool got = kSide == kSideWeights ? pop_unit(g, s, q, u) : push_unit(g, s, q, u);
+        if (!got || *s.abort_flag || !decode_unit(g, tv, u, un)) break;
         const CUtensorMap* wmap = un.phase == 1 ? &maps.w1 : (un.nw == 2 ? &maps.w2 : &maps.w2_one);
         const CUtensorMap* amap = un.phase == 1 ? &maps.xq[un.tbox] : &maps.hq[un.tbox];
         const uint8_t* wsf = un.phase == 1 ? g.w1_sf : g.w2_sf;
         const uint8_t* asf = un.phase == 1 ? g.xs_t : g.hs_t;
-        if (un.phase == 2) {
+        if (kTok && un.phase == 2) {
             const int need = g.I / kTile + (g.fault == kFaultGemmDependency ? 1 : 0);
             if (ld_acquire(&g.done1[un.tile]) < need) {
                 const uint64_t t0 = globaltimer();
@@ -343,15 +364,16 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
             fence_proxy_async_global();
             if (*s.abort_flag) break;
         }
-        const uint32_t bytes = (kBBox << un.tbox) * kKStep + un.nw * kWBoxTxBytes + (1 + un.nw) * kSFBytes;
+        const uint32_t bytes = (kTok ? (kBBox << un.tbox) * kKStep + kSFBytes : 0) +
+                               (kW ? un.nw * (kWBoxTxBytes + kSFBytes) : 0);
         const uint8_t* wblk = (un.phase == 1 ? g.w1 : g.w2) + static_cast<int64_t>(un.wz) * kWBoxTxBytes;
-        if (kPrefetch > 0) {
+        if (kW && kPrefetch > 0) {
             // the first stages of the unit; later ones are requested kPrefetch stages ahead
             for (int j = 1; j < kPrefetch && j < un.ksteps; ++j)
                 prefetch_l2(wblk + static_cast<int64_t>(2 * j) * kWBoxTxBytes, un.nw * kWBoxTxBytes);
         }
         for (int ks = 0; ks < un.ksteps; ++ks) {
-            if (kPrefetch > 0 && ks + kPrefetch < un.ksteps)
+            if (kW && kPrefetch > 0 && ks + kPrefetch < un.ksteps)
                 prefetch_l2(wblk + static_cast<int64_t>(2 * (ks + kPrefetch)) * kWBoxTxBytes, un.nw * kWBoxTxBytes);
             if (!mbar_wait(&s.empty[stage], phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
             uint8_t* st = s.stages + stage * G::kStageBytes;
@@ -360,11 +382,16 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
             armed[stage] = static_cast<int>(phase);
             // four copies per stage: token rows, token scales, the weight block
             // pair, the pair's scales
-            tma_load_2d(st, amap, ks * kKStep, un.row0, &s.full[stage], pol_a);
-            bulk_load(sf, asf + (static_cast<int64_t>(un.tile) * un.ksteps + ks) * kSFBytes, kSFBytes, &s.full[stage]);
-            const int wz = un.wz + 2 * ks;
-            tma_load_3d(st + G::kABytes, wmap, 0, 0, wz, &s.full[stage], pol_w);
-            bulk_load(sf + kSFBytes, wsf + static_cast<int64_t>(wz) * kSFBytes, un.nw * kSFBytes, &s.full[stage]);
+            if (kTok) {
+                tma_load_2d(st, amap, ks * kKStep, un.row0, &s.full[stage], pol_a);
+                bulk_load(sf, asf + (static_cast<int64_t>(un.tile) * un.ksteps + ks) * kSFBytes, kSFBytes,
+                          &s.full[stage]);
+            }
+            if (kW) {
+                const int wz = un.wz + 2 * ks;
+                tma_load_3d(st + G::kABytes, wmap, 0, 0, wz, &s.full[stage], pol_w);
+                bulk_load(sf + kSFBytes, wsf + static_cast<int64_t>(wz) * kSFBytes, un.nw * kSFBytes, &s.full[stage]);
+            }
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -372,10 +399,12 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
         }
     }
     if (*s.abort_flag) {
-        // let copies already in flight land before the CTA exits
+        // let copies already in flight land before the CTA exits.  (With a
+        // split producer a stage the other side never armed does not complete
+        // although this side's copies landed: one deadline for all stages.)
+        const uint64_t t0 = globaltimer();
         for (int i = 0; i < kStages; ++i) {
             if (armed[i] < 0) continue;
-            const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(&s.full[i], static_cast<uint32_t>(armed[i])))
                 if (globaltimer() - t0 > kWaitLimitNs / 4) break;
         }
@@ -499,8 +528,24 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16])
 // dec(u, un): the unit behind number u (false: none).  A unit whose tile is
 // absent (rows 0: the second CTA of a pair whose expert had an odd number of
 // tiles) is drained and released like any other, and writes nothing.
+// empty_remote: 0 = release the drained accumulator on this CTA's tmem_empty
+// (every epilogue thread arrives); otherwise the cluster address of the barrier
+// to arrive on: the second CTA of a pair reports straight to the CTA that
+// issues the pair's MMAs, one relaxed arrive per warp once all its lanes have
+// waited for their tensor-memory loads (nothing else needs ordering).
+__device__ __forceinline__ void release_acc(const GemmSmem& s, uint32_t empty_remote, int lane)
+{
+    if (empty_remote) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_peer_relaxed(empty_remote);
+    } else {
+        mbar_arrive(s.tmem_empty);
+    }
+}
+
 template <class Dec>
-__device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem& s, uint32_t tmem, const Dec& dec)
+__device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem& s, uint32_t tmem, const Dec& dec,
+                                              uint32_t empty_remote = 0)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;                       // TMEM lane quarter
@@ -534,7 +579,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem&
                 tmem_ld_wait();
             }
             tc_fence_before();
-            mbar_arrive(s.tmem_empty);
+            release_acc(s, empty_remote, lane);
             if (active && row_ok) {
                 const int64_t row = un.row0 + r;
                 const int col0 = un.blk * kTile + half * 64;            // first I-column of this half
@@ -586,7 +631,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem&
                 tmem_ld_wait();
             }
             tc_fence_before();
-            mbar_arrive(s.tmem_empty);
+            release_acc(s, empty_remote, lane);
             if (active && cols && row_ok) {
                 const int m0 = un.m0 + half * kTile;                                    // first output feature
                 uint4* dst = reinterpret_cast<uint4*>(g.y + static_cast<int64_t>(un.row0 + r) * g.H + m0);
@@ -606,14 +651,17 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem&
     }
 }
 
-// All threads: each warp runs its role over the units the CTA's producer draws.
-template <class G>
+// All threads: each warp runs its role over the units the CTA's producer draws
+// (kSplit: a block of kThreadsSplit threads, warp 10 the weight-side producer).
+template <class G, bool kSplit = false>
 __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                            const GemmSmem& s, uint32_t tmem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 0) {
-        if (lane == 0) producer_loop<G>(maps, g, tv, s);
+        if (lane == 0) producer_loop<G, kSplit ? kSideTokens : kSideBoth>(maps, g, tv, s);
+    } else if (warp == kWProdWarp) {
+        if (kSplit && lane == 0) producer_loop<G, kSideWeights>(maps, g, tv, s);
     } else if (warp == 1) {
         mma_loop<G>(g, tv, s, tmem);
     } else {

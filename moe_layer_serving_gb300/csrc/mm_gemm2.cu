@@ -18,14 +18,17 @@
 // second CTA without a tile in its last pair: that CTA loads only its half of
 // the weights, and its accumulator rows are never read.
 //
-// Roles: warp 0 lane 0 = producer (both CTAs: own token tile, own weight
-// half, the tile's scales and both halves' weight scales -- the MMA reads the
-// weight scales of all 256 columns in each CTA's tensor memory -- every copy
-// completing on CTA 0's barrier); warp 1 =
-// tensor-memory owner and, in CTA 0, the MMA issuer; in CTA 1 it reports its
-// drained accumulator to CTA 0 with a remote arrive;
-// warps 2..9 = epilogue.  Unit numbers are drawn by CTA 0 and handed to CTA 1,
-// so both run the same sequence.  Every wait is bounded.
+// Roles: warp 0 lane 0 = token-side producer (own token tile and its
+// scales), warp 10 lane 0 = weight-side producer (own weight half and both
+// halves' weight scales -- the MMA reads the weight scales of all 256 columns
+// in each CTA's tensor memory), in both CTAs, every copy completing on CTA 0's
+// barrier; warp 1 = tensor-memory owner and, in CTA 0, the MMA issuer (in CTA
+// 1 it only takes the unit numbers out of the ring); warps 2..9 = epilogue,
+// which in CTA 1 releases each drained accumulator with one relaxed remote
+// arrive per warp on CTA 0's peer_tmem_empty (relaying through a warp of CTA 1,
+// or arriving from every thread with release semantics, held the pair's MMAs
+// ~1,700 / ~2,000 cycles a unit).  Unit numbers are drawn by CTA 0's token-side producer and
+// handed to CTA 1's, so both run the same sequence.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -87,9 +90,15 @@ __device__ __forceinline__ bool decode2(const GemmArgs& g, int npairs, int u, ui
     return true;
 }
 
+// kSide: kSideTokens (draws or receives the unit numbers, waits for GEMM1
+// results before a GEMM2 unit) or kSideWeights (takes the numbers out of the
+// CTA's ring).  In CTA 0 each side arrives on the stage's full barrier with
+// the bytes of its side in both CTAs.
+template <int kSide>
 __device__ __forceinline__ void producer2(const GemmMaps& maps, const GemmArgs& g, int npairs, const GemmSmem& s,
                                           uint32_t rank)
 {
+    constexpr bool kTok = kSide == kSideTokens;
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
@@ -100,11 +109,12 @@ __device__ __forceinline__ void producer2(const GemmMaps& maps, const GemmArgs& 
     UnitQueue q, box;
     for (;;) {
         int u;
-        if (!push_unit(g, s, q, u, &box, rank) || *s.abort_flag || !decode2(g, npairs, u, rank, un)) break;
+        const bool got = kTok ? push_unit(g, s, q, u, &box, rank) : pop_unit(g, s, q, u);
+        if (!got || *s.abort_flag || !decode2(g, npairs, u, rank, un)) break;
         const bool has = un.rows > 0;
         const CUtensorMap* wmap = un.phase == 1 ? &maps.w1_one : &maps.w2_one;
         const CUtensorMap* amap = un.phase == 1 ? &maps.xq[un.tbox] : &maps.hq[un.tbox];
-        if (un.phase == 2 && has) {
+        if (kTok && un.phase == 2 && has) {
             const int need = g.I / kTile + (g.fault == kFaultGemmDependency ? 1 : 0);
             if (ld_acquire(&g.done1[un.tile]) < need) {
                 const uint64_t t0 = globaltimer();
@@ -125,22 +135,25 @@ __device__ __forceinline__ void producer2(const GemmMaps& maps, const GemmArgs& 
         // CTA 0's barrier counts the bytes of both: CTA 0's MMA waits on it
         // alone.  (CTA 1 reporting its own landed stages by remote arrives
         // measured 1.8x slower: the MMA warp woke late on each of them.)
-        uint32_t bytes = (has ? (kBBox << un.tbox) * kKStep + kSFBytes : 0) + kWBoxTxBytes + 2 * kSFBytes;
-        if (rank == 0) {
-            Unit peer;
-            if (!decode2(g, npairs, u, 1, peer)) break;
-            bytes += (peer.rows > 0 ? (kBBox << peer.tbox) * kKStep + kSFBytes : 0) + kWBoxTxBytes + 2 * kSFBytes;
+        uint32_t bytes = 2 * (kWBoxTxBytes + 2 * kSFBytes);
+        if (kTok) {
+            bytes = has ? (kBBox << un.tbox) * kKStep + kSFBytes : 0;
+            if (rank == 0) {
+                Unit peer;
+                if (!decode2(g, npairs, u, 1, peer)) break;
+                bytes += peer.rows > 0 ? (kBBox << peer.tbox) * kKStep + kSFBytes : 0;
+            }
         }
         const CUtensorMap* asf_map = un.phase == 1 ? &maps.xs_sf : &maps.hs_sf;
         const CUtensorMap* wsf_map = un.phase == 1 ? &maps.w1_sf : &maps.w2_sf;
         // this CTA's member of each stage's block pair
         const uint8_t* wblk = (un.phase == 1 ? g.w1 : g.w2) + static_cast<int64_t>(un.wz + rank) * kWBoxTxBytes;
-        if (kPrefetch > 0) {
+        if (!kTok && kPrefetch > 0) {
             for (int j = 1; j < kPrefetch && j < un.ksteps; ++j)
                 prefetch_l2(wblk + static_cast<int64_t>(2 * j) * kWBoxTxBytes, kWBoxTxBytes);
         }
         for (int ks = 0; ks < un.ksteps; ++ks) {
-            if (kPrefetch > 0 && ks + kPrefetch < un.ksteps)
+            if (!kTok && kPrefetch > 0 && ks + kPrefetch < un.ksteps)
                 prefetch_l2(wblk + static_cast<int64_t>(2 * (ks + kPrefetch)) * kWBoxTxBytes, kWBoxTxBytes);
             if (!mbar_wait(&s.empty[stage], phase ^ 1u, g.status, s.abort_flag, kSiteProducerEmpty)) break;
             uint8_t* st = s.stages + stage * kStage2Bytes;
@@ -151,12 +164,15 @@ __device__ __forceinline__ void producer2(const GemmMaps& maps, const GemmArgs& 
                 mbar_arrive_expect_tx(&s.full[stage], bytes);
                 armed[stage] = static_cast<int>(phase);
             }
-            if (has) {
-                tma_load_2d_pair(st, amap, ks * kKStep, un.row0, bar, pol_a);
-                tma_load_2d_pair(sf, asf_map, 0, 2 * (un.tile * un.ksteps + ks), bar, pol_a);
+            if (kTok) {
+                if (has) {
+                    tma_load_2d_pair(st, amap, ks * kKStep, un.row0, bar, pol_a);
+                    tma_load_2d_pair(sf, asf_map, 0, 2 * (un.tile * un.ksteps + ks), bar, pol_a);
+                }
+            } else {
+                tma_load_3d_pair(st + kA2Bytes, wmap, 0, 0, wz + static_cast<int>(rank), bar, pol_w);
+                tma_load_2d_pair(sf + kSFBytes, wsf_map, 0, 2 * wz, bar, pol_w);
             }
-            tma_load_3d_pair(st + kA2Bytes, wmap, 0, 0, wz + static_cast<int>(rank), bar, pol_w);
-            tma_load_2d_pair(sf + kSFBytes, wsf_map, 0, 2 * wz, bar, pol_w);
             if (++stage == kStages2) {
                 stage = 0;
                 phase ^= 1u;
@@ -164,9 +180,11 @@ __device__ __forceinline__ void producer2(const GemmMaps& maps, const GemmArgs& 
         }
     }
     if (*s.abort_flag) {
+        // (one deadline for all stages: a stage the other side never armed
+        // does not complete although this side's copies landed)
+        const uint64_t t0 = globaltimer();
         for (int i = 0; i < kStages2; ++i) {
             if (armed[i] < 0) continue;
-            const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(&s.full[i], static_cast<uint32_t>(armed[i])))
                 if (globaltimer() - t0 > kWaitLimitNs / 4) break;
         }
@@ -254,14 +272,11 @@ __device__ __forceinline__ void mma2_loop(const GemmArgs& g, int npairs, const G
     }
 }
 
-// Warp 1 of CTA 1: from the second unit on, report this CTA's drained
-// accumulator to CTA 0 (a remote arrive, one lane).
+// Warp 1 of CTA 1: takes the unit numbers out of the ring (one of its
+// consumers), nothing else.
 __device__ __forceinline__ void relay_loop(const GemmArgs& g, int npairs, const GemmSmem& s)
 {
     const int lane = threadIdx.x & 31;
-    const uint32_t peer_tmem_empty = peer_addr(s.peer_tmem_empty, 0);
-    uint32_t acc_phase = 0;
-    bool first = true;
     Unit un;
     UnitQueue q;
     for (;;) {
@@ -272,20 +287,10 @@ __device__ __forceinline__ void relay_loop(const GemmArgs& g, int npairs, const 
         if (lane == 0) mbar_arrive(&s.uempty[q.slot]);
         q.advance();
         if (*s.abort_flag || !decode2(g, npairs, u, 1, un)) break;
-        if (!first) {
-            // this CTA's epilogue drained the previous unit's accumulator
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(s.tmem_empty, acc_phase ^ 1u, g.status, s.abort_flag,
-                                                   kSiteMmaTmemEmpty)))
-                break;
-            if (lane == 0) mbar_arrive_peer(peer_tmem_empty);
-            __syncwarp();
-        }
-        first = false;
-        acc_phase ^= 1u;
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsSplit, 1)
     gemm2_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -295,16 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages2; ++i) {
-            mbar_init(&s.full[i], 1);
+            mbar_init(&s.full[i], 2);          // CTA 0's: both producer sides arrive
             mbar_init(&s.empty[i], 1);
         }
         mbar_init(s.tmem_full, 1);
         mbar_init(s.tmem_empty, kEpiThreads);
-        mbar_init(s.peer_tmem_empty, 1);
+        mbar_init(s.peer_tmem_empty, kEpiThreads / 32);   // one arrive per epilogue warp of CTA 1
         mbar_init(s.drain, 1);
         for (int i = 0; i < kURing; ++i) {
             mbar_init(&s.ufull[i], 1);
-            mbar_init(&s.uempty[i], 1 + kEpiThreads);
+            mbar_init(&s.uempty[i], 2 + kEpiThreads);
             mbar_init(&s.inbox_full[i], 1);
             mbar_init(&s.inbox_free[i], 1);
         }
@@ -323,14 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *s.tmem_slot;
     const int npairs = g.num_tiles[2];
     if (warp == 0) {
-        if (lane == 0) producer2(maps, g, npairs, s, rank);
+        if (lane == 0) producer2<kSideTokens>(maps, g, npairs, s, rank);
+    } else if (warp == kWProdWarp) {
+        if (lane == 0) producer2<kSideWeights>(maps, g, npairs, s, rank);
     } else if (warp == 1) {
         if (rank == 0)
             mma2_loop(g, npairs, s, tmem);
         else
             relay_loop(g, npairs, s);
     } else {
-        epilogue_loop(g, s, tmem, [&](int u, Unit& un) { return decode2(g, npairs, u, rank, un); });
+        epilogue_loop(g, s, tmem, [&](int u, Unit& un) { return decode2(g, npairs, u, rank, un); },
+                      rank == 1 ? peer_addr(s.peer_tmem_empty, 0) : 0u);
     }
     // neither CTA frees tensor memory or exits before the pair is done with it
     tc_fence_before();
@@ -354,7 +362,7 @@ cudaError_t gemm2_prepare(int dev)
     if (dev >= 0 && dev < 64 && g_clusters2[dev] == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2);
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(kThreadsSplit);
         cfg.dynamicSmemBytes = kSmem2Bytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -386,7 +394,7 @@ cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s)
     const int clusters = g_clusters2[c->dev] < c->sms / 2 ? g_clusters2[c->dev] : c->sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsSplit);
     cfg.dynamicSmemBytes = kSmem2Bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

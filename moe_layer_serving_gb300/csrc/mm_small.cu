@@ -28,7 +28,10 @@
 namespace mm {
 namespace {
 
-constexpr int kSmallWarps = kThreads / 32;
+// The GEMM phase runs the split producer (token side in warp 0, weight side in
+// warp 10), so the block has kThreadsSplit threads and every phase uses them.
+constexpr int kSmallThreads = kThreadsSplit;
+constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
 // Two pipeline geometries over one buffer: short tiles with one more stage
 // when every expert's rows fit in few short tiles (weight streaming, where the
@@ -145,7 +148,7 @@ __device__ bool grid_sync(unsigned* bar, int* status, volatile int* abort_flag, 
     return !*abort_flag;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSmallThreads, 1)
     small_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g,
                  const __grid_constant__ SmallArgs a)
 {
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* t_rows = t_row0 + kMaxSmallTiles;
     int* scal = t_rows + kMaxSmallTiles;            // [0] tiles, [1] rows, [2] [3] tile counts
     static_assert(GeomSmall::kStages >= GeomLarge::kStages, "barriers initialised for the deeper pipeline");
-    const uint32_t tmem = gemm_setup<GeomSmall>(s, maps);
+    const uint32_t tmem = gemm_setup<GeomSmall, true>(s, maps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = a.route.T;
@@ -199,20 +202,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lt = (1u << lane) - 1u;
     if (ok) {
         // the pairs' physical experts: each thread issues its loads before storing
-        for (int i0 = threadIdx.x; i0 < N; i0 += 8 * kThreads) {
+        for (int i0 = threadIdx.x; i0 < N; i0 += 8 * kSmallThreads) {
             int v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * kThreads;
+                const int i = i0 + u * kSmallThreads;
                 v[u] = i < N ? a.route.phys[i] : 0;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * kThreads;
+                const int i = i0 + u * kSmallThreads;
                 if (i < N) sphys[i] = v[u];
             }
         }
-        for (int i = threadIdx.x; i < kSmallWarps * MM_MAX_EXPERTS; i += kThreads) wcnt[i] = 0;
+        for (int i = threadIdx.x; i < kSmallWarps * MM_MAX_EXPERTS; i += kSmallThreads) wcnt[i] = 0;
         __syncthreads();
         int* wc = wcnt + warp * MM_MAX_EXPERTS;
         for (int base = lo; base < hi; base += 32) {
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
         __syncthreads();
-        for (int p = threadIdx.x; p < P; p += kThreads) {
+        for (int p = threadIdx.x; p < P; p += kSmallThreads) {
             int run = 0;
             for (int w = 0; w < kSmallWarps; ++w) {
                 const int v = wcnt[w * MM_MAX_EXPERTS + p];
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile counts in both tile sizes (thread i takes experts [i * per,
             // i * per + per)); the totals choose the tile size: short tiles
             // unless they would add more than 1/16 to the tile count
-            const int per = (P + kThreads - 1) / kThreads;
+            const int per = (P + kSmallThreads - 1) / kSmallThreads;
             const int p0 = min(P, static_cast<int>(threadIdx.x) * per), p1 = min(P, p0 + per);
             int v[kScanVals] = {0, 0, 0};
             for (int p = p0; p < p1; ++p) {
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        for (int p = threadIdx.x; p < P; p += kThreads) {
+        for (int p = threadIdx.x; p < P; p += kSmallThreads) {
             const int nt = tiles_of(cnt[p], tile);
             for (int t = 0; t < nt; ++t) {
                 t_expert[stoff[p] + t] = p;
@@ -290,9 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (blockIdx.x == 0) {
-            for (int i = threadIdx.x; i < N; i += kThreads) a.pos[i] = spos[i];
-            for (int p = threadIdx.x; p <= P; p += kThreads) a.off[p] = soff[p];
-            for (int t = threadIdx.x; t < scal[0]; t += kThreads) {
+            for (int i = threadIdx.x; i < N; i += kSmallThreads) a.pos[i] = spos[i];
+            for (int p = threadIdx.x; p <= P; p += kSmallThreads) a.off[p] = soff[p];
+            for (int t = threadIdx.x; t < scal[0]; t += kSmallThreads) {
                 a.tile_expert[t] = t_expert[t];
                 a.tile_row0[t] = t_row0[t];
                 a.tile_rows[t] = t_rows[t];
@@ -306,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- D: MXFP8 quantisation + dispatch ------------------------------
         const int nb = H / 32;
-        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < T * nb;
-             it += static_cast<int64_t>(gridDim.x) * kThreads) {
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kSmallThreads + threadIdx.x; it < T * nb;
+             it += static_cast<int64_t>(gridDim.x) * kSmallThreads) {
             const int64_t t = it / nb;
             quant_dispatch_block(a.x, t, static_cast<int>(it % nb), H, k, spos + t * k, sphys + t * k, soff, stoff,
                                  tile, a.xq, a.xs_t, chk);
@@ -327,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tv.rows = t_rows;
         tv.ntiles = scal[0];
         if (short_tiles)
-            gemm_roles<GeomSmall>(maps, g, tv, s, tmem);
+            gemm_roles<GeomSmall, true>(maps, g, tv, s, tmem);
         else
-            gemm_roles<GeomLarge>(maps, g, tv, s, tmem);
+            gemm_roles<GeomLarge, true>(maps, g, tv, s, tmem);
     }
     gemm_teardown(tmem);
     if (threadIdx.x == 0) stamp[5] = globaltimer();
@@ -339,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- H: combine ---------------------------------------------------------
     if (ok) {
         const int nc = H / 8;
-        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < T * nc;
-             it += static_cast<int64_t>(gridDim.x) * kThreads)
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kSmallThreads + threadIdx.x; it < T * nc;
+             it += static_cast<int64_t>(gridDim.x) * kSmallThreads)
             combine_chunk(g.y, a.route.w, a.pos, it / nc, static_cast<int>(it % nc), H, k, a.out, chk);
     }
     __syncthreads();
@@ -393,7 +396,7 @@ cudaError_t launch_small(const mm_ctx* c, const void* hidden, const float* logit
     a.P = pw(c);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c->sms));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kSmallThreads);
     cfg.dynamicSmemBytes = kSmallSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
