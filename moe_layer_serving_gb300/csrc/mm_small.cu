@@ -32,6 +32,7 @@ namespace {
 // warp 10), so the block has kThreadsSplit threads and every phase uses them.
 constexpr int kSmallThreads = kThreadsSplit;
 constexpr int kSmallWarps = kSmallThreads / 32;
+static_assert(kSmallThreads % 4 == 0, "quant_dispatch_block takes four consecutive lanes per K chunk");
 constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
 // Two pipeline geometries over one buffer: short tiles with one more stage
 // when every expert's rows fit in few short tiles (weight streaming, where the

@@ -220,6 +220,10 @@ __device__ __forceinline__ uint8_t quant_block32(const __nv_bfloat16* __restrict
 // dispatch rows and physical experts of token t; off / toff: segment start row
 // and first token tile of each expert (global or shared memory), which place
 // the scale byte in the scale tile of the row's token tile.
+// Callers map four consecutive lanes (lane % 4 == b % 4) to the four blocks of
+// one 128-wide K chunk of one token, all four active together: their scale
+// bytes are adjacent in the scale tile, so the first lane of the four stores
+// them as one word instead of four byte stores.
 __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __restrict__ x, int64_t t, int b, int H,
                                                      int k, const int32_t* pos_t, const int32_t* phys_t,
                                                      const int32_t* off, const int32_t* toff, int tile,
@@ -228,7 +232,13 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
 {
     (void)chk;
     uint32_t packed[8];
-    const uint8_t sbyte = quant_block32(x, t, b, H, packed);
+    const uint32_t sbyte = quant_block32(x, t, b, H, packed);
+    const int lane = threadIdx.x & 31;
+    const unsigned group = 0xFu << (lane & ~3);
+    uint32_t sword = sbyte;
+    sword |= __shfl_down_sync(group, sbyte, 1, 4) << 8;
+    sword |= __shfl_down_sync(group, sbyte, 2, 4) << 16;
+    sword |= __shfl_down_sync(group, sbyte, 3, 4) << 24;
     const int kchunks = H / 128;
     for (int j = 0; j < k; ++j) {
         const int64_t row = pos_t[j];
@@ -237,8 +247,10 @@ __device__ __forceinline__ void quant_dispatch_block(const __nv_bfloat16* __rest
         uint4* dst = reinterpret_cast<uint4*>(xq + row * H + b * 32);
         dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        const int rank = static_cast<int>(row) - off[p];
-        xs_t[act_sf_offset(toff[p] + rank / tile, rank % tile, b, kchunks)] = sbyte;
+        if ((b & 3) == 0) {
+            const int rank = static_cast<int>(row) - off[p];
+            *reinterpret_cast<uint32_t*>(xs_t + act_sf_offset(toff[p] + rank / tile, rank % tile, b, kchunks)) = sword;
+        }
     }
 }
 
