@@ -217,7 +217,11 @@ MM_API mm_status mm_debug_dump(mm_handle h, int stage, void *dst_host, size_t by
  * (1 small, 2 large), number of kernels it launched, site of the last
  * device-side timeout or check (0 none; see WaitSite in the sources), the
  * grouped GEMM kernel of the large path (0 none, 1 one CTA per unit, 2 CTA
- * pairs with 2-SM MMAs, 3 the a16w4 kernel)}.
+ * pairs with 2-SM MMAs, 3 the a16w4 kernel)}.  By default both a8w4 kernels
+ * are launched and the tile scan picks one on the device: the pair kernel when
+ * the experts' odd tile counts add at most 1/64 to the MMA work (environment
+ * MM_GEMM_2SM=0 or 1 fixes the one-CTA or the pair kernel); the entry then
+ * names the kernel that ran and the launch count includes the other.
  * Stage 11: uint64 [SMs][8] %globaltimer readings (ns) of each CTA of the last
  * fused small-input launch at its stage boundaries: start, routed, past
  * barrier 1, dispatched, past barrier 2, GEMMs done, past barrier 3, end.

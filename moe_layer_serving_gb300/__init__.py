@@ -305,7 +305,9 @@ class MegaMoE:
 
     def last_gemm(self) -> int:
         """Grouped GEMM kernel of the last forward: 0 none (fused small-input
-        kernel), 1 one CTA per unit, 2 CTA pairs (2-SM MMAs), 3 a16w4."""
+        kernel), 1 one CTA per unit, 2 CTA pairs (2-SM MMAs), 3 a16w4.  (By
+        default the large path launches both a8w4 kernels and the tile scan
+        picks one on the device; this names the one that ran.)"""
         return int(self.debug_dump(10)[3])
 
     def debug_dump(self, stage: int) -> np.ndarray:

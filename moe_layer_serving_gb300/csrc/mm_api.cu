@@ -187,7 +187,8 @@ mm_status mm_create(int E, int P, int k, int H, int I, mm_handle* out)
     c->small_max = env_int("MM_SMALL_M_MAX", mm::kSmallMaxTokens);
     if (c->small_max > mm::kSmallMaxTokens) c->small_max = mm::kSmallMaxTokens;
     c->large_min = env_int("MM_LARGE_M_MIN", 1024);
-    c->gemm_2sm = env_int("MM_GEMM_2SM", 0) != 0;
+    c->gemm_2sm = env_int("MM_GEMM_2SM", 2);        // 0 one CTA, 1 CTA pairs, 2 chosen per batch
+    if (c->gemm_2sm < 0 || c->gemm_2sm > 2) c->gemm_2sm = 2;
     if (mm::gemm_prepare(dev) != cudaSuccess || mm::gemm2_prepare(dev) != cudaSuccess ||
         mm::small_prepare() != cudaSuccess ||
         mm::gemm16_prepare() != cudaSuccess ||
@@ -609,8 +610,8 @@ mm_status mm_forward(mm_handle c, const void* hidden, const float* logits, const
     }
     if (prof) ++c->prof_used;
     c->last_route = small ? 1 : 2;
-    c->last_launches = small ? 1 : 7;
-    c->last_gemm = small ? 0 : (mm::gemm2_usable(c) ? 2 : 1);
+    c->last_gemm = small ? 0 : mm::gemm_kind(c);
+    c->last_launches = small ? 1 : (c->last_gemm == 4 ? 8 : 7);
     c->last_T = T;
     c->last_stream = s;
     return MM_OK;
@@ -729,7 +730,14 @@ mm_status mm_debug_dump(mm_handle c, int stage, void* dst, size_t bytes)
     if (stage == 10) {
         int32_t site = 0;
         CK(cudaMemcpy(&site, c->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost));
-        const int32_t info[4] = {c->last_route, c->last_launches, site ? site : c->last_site, c->last_gemm};
+        int32_t kind = c->last_gemm;
+        if (kind == 4) {
+            // both large-input GEMM kernels were launched; the tile scan chose one
+            int32_t pairs = 0;
+            CK(cudaMemcpy(&pairs, c->num_tiles + 3, sizeof(int32_t), cudaMemcpyDeviceToHost));
+            kind = pairs ? 2 : 1;
+        }
+        const int32_t info[4] = {c->last_route, c->last_launches, site ? site : c->last_site, kind};
         memcpy(dst, info, n);
         return MM_OK;
     }

@@ -16,6 +16,9 @@ constexpr int kSmemBytes = Geo::kSmemBytes + 1024;
 __global__ void __launch_bounds__(kThreadsSplit, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g)
 {
+    // the batch went to the pair kernel (launched after this one): every CTA
+    // reads the same choice and returns before touching anything
+    if (g.select == 1 && g.num_tiles[3] != 0) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const GemmSmem s = gemm_smem(smem, smem + Geo::kStageRegion);
@@ -63,14 +66,17 @@ void fill_gemm_args(const mm_ctx* c, GemmArgs* gp)
     g.rows_cap = static_cast<int>(c->rows_cap);
     g.st_tile = c->st_tile;
     g.keep_weights = 0;
+    g.select = 0;
 }
 
 cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)
 {
     (void)T;
-    if (gemm2_usable(c)) return launch_gemm2(c, s);
+    const bool pairs = gemm2_usable(c);
+    if (pairs && c->gemm_2sm == 1) return launch_gemm2(c, s, 0);
     GemmArgs g;
     fill_gemm_args(c, &g);
+    g.select = pairs ? 1 : 0;       // gemm_2sm == 2: the tile scan chooses on the device
     // Large batches give an expert several token tiles, each re-reading the
     // expert's weight blocks: loading them with the normal L2 policy rather
     // than evict-first measured 2% faster on the skewed 16384-token layer (its
@@ -86,7 +92,15 @@ cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel, c->maps, g);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, c->maps, g);
+    if (e != cudaSuccess || !pairs) return e;
+    return launch_gemm2(c, s, 2);
+}
+
+int gemm_kind(const mm_ctx* c)
+{
+    if (!gemm2_usable(c)) return 1;
+    return c->gemm_2sm == 1 ? 2 : 4;
 }
 
 }  // namespace mm

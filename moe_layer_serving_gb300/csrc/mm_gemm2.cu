@@ -293,6 +293,9 @@ __device__ __forceinline__ void relay_loop(const GemmArgs& g, int npairs, const 
 __global__ void __launch_bounds__(kThreadsSplit, 1)
     gemm2_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g)
 {
+    // the batch went to the one-CTA kernel (launched before this one): every
+    // CTA of every pair reads the same choice and returns before any barrier
+    if (g.select == 2 && g.num_tiles[3] == 0) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const GemmSmem s = gemm_smem(smem, smem + kStageRegion2);
@@ -384,13 +387,14 @@ cudaError_t gemm2_prepare(int dev)
 bool gemm2_usable(const mm_ctx* c)
 {
     // every GEMM2 unit a full pair of 128-row weight blocks
-    return c->gemm_2sm && c->dev >= 0 && c->dev < 64 && g_clusters2[c->dev] > 0 && c->H % (2 * kTile) == 0;
+    return c->gemm_2sm != 0 && c->dev >= 0 && c->dev < 64 && g_clusters2[c->dev] > 0 && c->H % (2 * kTile) == 0;
 }
 
-cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s)
+cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s, int select)
 {
     GemmArgs g;
     fill_gemm_args(c, &g);
+    g.select = select;
     const int clusters = g_clusters2[c->dev] < c->sms / 2 ? g_clusters2[c->dev] : c->sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));

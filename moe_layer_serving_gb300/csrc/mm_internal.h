@@ -170,7 +170,14 @@ struct GemmArgs {
     const int* st_tile;     // the 2-SM GEMM's tile pairs [2 * num_tiles[2]]
     int keep_weights;       // 1: weight loads with the normal L2 policy (an expert's tiles re-read its
                             // weights); 0: evict-first (streamed once, the fused small-input kernel)
+    int select;             // 0: run; 1: run unless num_tiles[3] chose the pair kernel; 2: run only if it did
 };
+
+// The tile scan's choice between the large-input GEMM kernels (num_tiles[3]):
+// the pair kernel gives each pair of an expert's tiles one M = 256 MMA, so an
+// expert with an odd tile count costs it a whole extra tile of MMA work; it is
+// chosen when those extra tiles are at most 1/64 of all tiles.
+__host__ __device__ inline int choose_pairs(int tiles, int pairs) { return (2 * pairs - tiles) * 64 <= tiles ? 1 : 0; }
 
 }  // namespace mm
 
@@ -181,7 +188,10 @@ struct mm_ctx {
     int small_max = 512, large_min = 1024;
     int route = MM_ROUTE_AUTO, layer = 0, recording = 0;
     int fault = 0;                  // mm::FaultSite
-    bool gemm_2sm = false;          // large-input GEMM on CTA pairs when the shapes allow (MM_GEMM_2SM=1)
+    // large-input GEMM kernel (MM_GEMM_2SM): 0 one CTA per unit, 1 CTA pairs
+    // (2-SM MMAs) when the shapes allow, 2 chosen per batch on the device from
+    // the tile counts (both kernels are launched; the one not chosen returns)
+    int gemm_2sm = 2;
     // weights (library-owned)
     uint8_t *w1 = nullptr, *w1_sf = nullptr, *w2 = nullptr, *w2_sf = nullptr;
     bool weights_set = false;
@@ -289,8 +299,11 @@ cudaError_t launch_tile_scales(const uint8_t* src, uint8_t* dst, int64_t rows, i
 cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t rows, int K, WOrder o, cudaStream_t s);
 cudaError_t gemm_prepare(int dev);
 cudaError_t gemm2_prepare(int dev);
-bool gemm2_usable(const mm_ctx* c);        // the large-input GEMM runs on CTA pairs for this handle
-cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s);
+bool gemm2_usable(const mm_ctx* c);        // the large-input GEMM may run on CTA pairs for this handle
+cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s, int select);   // select: GemmArgs::select
+// the large-input GEMM launch_gemm runs: 1 one CTA per unit, 2 CTA pairs, 4 chosen on the device (read
+// num_tiles[3]: 0 one CTA, 1 pairs)
+int gemm_kind(const mm_ctx* c);
 cudaError_t gemm16_prepare();
 cudaError_t launch_gemm16(const mm_ctx* c, cudaStream_t s);
 cudaError_t launch_dispatch16(const mm_ctx* c, const void* hidden, int64_t T, cudaStream_t s);

@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(512) scan_kernel(ScanArgs a)
             a.num_tiles[0] = tiles_incl;
             a.num_tiles[1] = 0;
             a.num_tiles[2] = pairs_incl;
+            a.num_tiles[3] = choose_pairs(tiles_incl, pairs_incl);
         }
     }
 }

@@ -74,7 +74,10 @@ def test_forced_routes_agree(torch):
     hidden, logits, bias = synthetic.make_activations(cfg, 200)
     run = gpu_util.Run(cfg, cap=200)
     outs = []
-    for r, expect in ((mm.ROUTE_SMALL, (1, 1)), (mm.ROUTE_LARGE, (2, 7)), (mm.ROUTE_AUTO, (1, 1))):
+    # the large route: route, hist, scan, scatter, quantise/dispatch, the two
+    # grouped GEMM kernels (H = 256 allows CTA pairs: both are launched, the
+    # tile scan picks one), combine
+    for r, expect in ((mm.ROUTE_SMALL, (1, 1)), (mm.ROUTE_LARGE, (2, 8)), (mm.ROUTE_AUTO, (1, 1))):
         run.op.set_route(r)
         outs.append(run.forward(hidden, logits, bias, dumps=False)["out"])
         route, launches, site = run.op.last_info()

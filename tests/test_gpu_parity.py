@@ -274,3 +274,43 @@ def test_two_sm_gemm_matches_one_cta_gemm(H, I, T, E, k):
     for name in ("hq", "hs", "y", "out"):
         assert np.array_equal(res["1"][name], res["0"][name]), name
     gpu_util.check_against_oracle(cfg, res["1"], hidden, logits, bias, W, None, gpu_util.tile_edge_tokens(res["1"], T))
+
+
+@pytest.mark.parametrize("T,kind", [(1024, 2), (400, 1)])
+def test_gemm_kernel_chosen_per_batch(T, kind):
+    # By default both large-input GEMM kernels are launched and the tile scan
+    # picks one per batch on the device: the pair kernel when the experts' odd
+    # tile counts add at most 1/64 to its MMA work.  Token t goes to experts
+    # t % 8 and (t + 1) % 8: at T = 1024 every expert has two full tiles (the
+    # pairs are chosen), at T = 400 every expert has one tile of 100 rows (the
+    # one-CTA kernel is).  The default run equals the fixed choice bit for bit.
+    import dataclasses
+    import os
+    cfg = dataclasses.replace(synthetic.CONFIGS[0], T=T, H=512, I=256, E=8, P=8, k=2)
+    hidden, _, _ = synthetic.make_activations(cfg)
+    logits = np.full((T, cfg.E), -8.0, np.float32)
+    t = np.arange(T)
+    logits[t, t % 8] = 6.0
+    logits[t, (t + 1) % 8] = 5.0
+    bias = np.zeros(cfg.E, np.float32)
+    W = synthetic.make_all_weights(cfg)
+    res = {}
+    for mode in (None, str(kind - 1)):
+        if mode is not None:
+            os.environ["MM_GEMM_2SM"] = mode
+        try:
+            run = gpu_util.Run(cfg, W, cap=T)
+        finally:
+            os.environ.pop("MM_GEMM_2SM", None)
+        run.op.set_route(2)
+        res[mode] = run.forward(hidden, logits, bias)
+        info = run.op.debug_dump(10)
+        run.close()
+        assert res[mode]["status"] == 0
+        assert int(info[3]) == kind
+        assert int(info[1]) == (8 if mode is None else 7)      # the default launches both kernels
+    per_expert = np.bincount(res[None]["tiles"].reshape(-1, 3)[:, 0], minlength=cfg.P)
+    assert np.all(per_expert == (2 if kind == 2 else 1))
+    for name in ("hq", "hs", "y", "out"):
+        assert np.array_equal(res[None][name], res[str(kind - 1)][name]), name
+    gpu_util.check_against_oracle(cfg, res[None], hidden, logits, bias, W, None, gpu_util.tile_edge_tokens(res[None], T))
