@@ -32,26 +32,34 @@ def torch():
     return torch
 
 
-def _faulty_run(cfg, T, fault, act=0):
+def _faulty_run(cfg, T, fault, act=0, gemm=None):
     os.environ["MM_FAULT"] = fault
+    if gemm is not None:
+        os.environ["MM_GEMM_2SM"] = gemm
     try:
         run = gpu_util.Run(cfg, cap=T, act=act)
     finally:
         del os.environ["MM_FAULT"]
+        os.environ.pop("MM_GEMM_2SM", None)
     hidden, logits, bias = synthetic.make_activations(cfg, T)
     res = run.forward(hidden, logits, bias, dumps=False)
     route, _, site = run.op.last_info()
+    kind = run.op.last_gemm()
     run.close()
+    if gemm is not None and route == 2:
+        assert kind == int(gemm) + 1          # the GEMM kernel the test means to time out
     return res["status"], route, site, (hidden, logits, bias)
 
 
-@pytest.mark.parametrize("fault,T,site,route", [("grid_barrier", 64, SITE_GRID_BARRIER, 1),
-                                                ("gemm_dependency", 64, SITE_PRODUCER_DONE1, 1),
-                                                ("gemm_dependency", 1200, SITE_PRODUCER_DONE1, 2)])
-def test_injected_wait_times_out_and_context_survives(torch, fault, T, site, route):
+@pytest.mark.parametrize("fault,T,site,route,gemm", [("grid_barrier", 64, SITE_GRID_BARRIER, 1, None),
+                                                     ("gemm_dependency", 64, SITE_PRODUCER_DONE1, 1, None),
+                                                     ("gemm_dependency", 1200, SITE_PRODUCER_DONE1, 2, "0"),
+                                                     ("gemm_dependency", 1200, SITE_PRODUCER_DONE1, 2, "1")])
+def test_injected_wait_times_out_and_context_survives(torch, fault, T, site, route, gemm):
+    # gemm: MM_GEMM_2SM for the large path ("0" the one-CTA kernel, "1" CTA pairs)
     import moe_layer_serving_gb300 as mm
     cfg = synthetic.CONFIGS[0]
-    status, took, got_site, inputs = _faulty_run(cfg, T, fault)
+    status, took, got_site, inputs = _faulty_run(cfg, T, fault, gemm=gemm)
     assert took == route
     assert status == mm.MM_ERR_TIMEOUT
     assert got_site == site
