@@ -13,7 +13,7 @@ namespace {
 using Geo = GeomLarge;
 constexpr int kSmemBytes = Geo::kSmemBytes + 1024;
 
-__global__ void __launch_bounds__(kThreadsSplit, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g)
 {
     // the batch went to the pair kernel (launched after this one): every CTA
@@ -22,13 +22,13 @@ __global__ void __launch_bounds__(kThreadsSplit, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const GemmSmem s = gemm_smem(smem, smem + Geo::kStageRegion);
-    const uint32_t tmem = gemm_setup<Geo, true>(s, maps);
+    const uint32_t tmem = gemm_setup<Geo>(s, maps);
     TileView tv;
     tv.expert = g.tile_expert;
     tv.row0 = g.tile_row0;
     tv.rows = g.tile_rows;
     tv.ntiles = *g.num_tiles;
-    gemm_roles<Geo, true>(maps, g, tv, s, tmem);
+    gemm_roles<Geo>(maps, g, tv, s, tmem);
     gemm_teardown(tmem);
 }
 
@@ -84,7 +84,7 @@ cudaError_t launch_gemm(const mm_ctx* c, int64_t T, cudaStream_t s)
     g.keep_weights = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c->sms));
-    cfg.blockDim = dim3(kThreadsSplit);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

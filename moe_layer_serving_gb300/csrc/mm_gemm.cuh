@@ -26,17 +26,18 @@
 // GEMM2 units, so a fixed round-robin split leaves some SMs a whole GEMM1 unit
 // behind).  All GEMM1 units precede all GEMM2 units, and a GEMM2 unit waits
 // (bounded) until the GEMM1 units of its tile have published hq.  Warp roles:
-// 0 = TMA producer (one lane), 1 = tensor-memory owner + MMA issuer (the whole
-// warp, one elected lane issuing), 2..9 = epilogue.
+// 0 = token-side TMA producer (one lane; it also draws the units), 10 =
+// weight-side TMA producer (one lane), 1 = tensor-memory owner + MMA issuer
+// (the whole warp, one elected lane issuing), 2..9 = epilogue.
 //
 // Issuing a stage's copies takes one thread about 500 cycles (each bulk copy
 // ~130, each tensor copy ~60, the expect-tx arrive and the L2 prefetch more),
 // about as long as the stage's MMAs (555 cycles), so a single producer thread
-// cannot get ahead of the tensor cores again after a late stage.  The
-// large-input kernels therefore split the producer: warp 0 issues the token
-// side (token rows and their scales) and draws the units, warp 10 the weight
-// side (weight blocks, their scales, the L2 prefetch); each arrives on the
-// stage's full barrier with its own byte count.  The eight epilogue warps
+// cannot get ahead of the tensor cores again after a late stage.  The producer
+// is therefore split: the token side issues the token rows and their scales,
+// the weight side the weight blocks, their scales and the L2 prefetch, and
+// each arrives on the stage's full barrier with its own byte count.  The eight
+// epilogue warps
 // first drain the accumulator into registers (each warp: its 32 token rows,
 // half of the columns) and release tensor memory, so the next unit's MMAs run
 // while they compute.
@@ -52,9 +53,8 @@
 
 namespace mm {
 
-constexpr int kThreads = 320;              // 10 warps
-constexpr int kWProdWarp = 10;             // the weight-side producer of a split kernel
-constexpr int kThreadsSplit = kThreads + 32;
+constexpr int kThreads = 352;              // 11 warps
+constexpr int kWProdWarp = 10;             // the weight-side producer
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -212,14 +212,14 @@ __device__ __forceinline__ GemmSmem gemm_smem(uint8_t* stages, uint8_t* bars)
     return s;
 }
 
-// All threads: barriers, tensor-memory allocation (warp 1); returns the TMEM base.
-// kSplit: two producer threads (token side and weight side) arrive on every
-// full barrier and take every unit out of the ring.
-template <class G, bool kSplit = false>
+// All threads: barriers, tensor-memory allocation (warp 1); returns the TMEM
+// base.  Both producer threads (token side and weight side) arrive on every
+// full barrier; the weight side takes every unit out of the ring.
+template <class G>
 __device__ __forceinline__ uint32_t gemm_setup(const GemmSmem& s, const GemmMaps& maps)
 {
     const int warp = threadIdx.x >> 5;
-    constexpr uint32_t kProducers = kSplit ? 2 : 1;
+    constexpr uint32_t kProducers = 2;
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::kStages; ++i) {
             mbar_init(&s.full[i], kProducers);
@@ -320,17 +320,17 @@ __device__ __forceinline__ bool pop_unit(const GemmArgs& g, const GemmSmem& s, U
     return true;
 }
 
-// ---- producer -----------------------------------------------------------------
-// kSide 0: one thread issues every copy; 1: the token side (draws the units,
-// waits for GEMM1 results before a GEMM2 unit); 2: the weight side (takes the
-// units out of the ring like the consumers).
-constexpr int kSideBoth = 0, kSideTokens = 1, kSideWeights = 2;
+// ---- producers ----------------------------------------------------------------
+// kSideTokens: the token side (draws the units, waits for GEMM1 results before
+// a GEMM2 unit); kSideWeights: the weight side (takes the units out of the
+// ring like the consumers).
+constexpr int kSideTokens = 1, kSideWeights = 2;
 
-template <class G, int kSide = kSideBoth>
+template <class G, int kSide>
 __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                               const GemmSmem& s)
 {
-    constexpr bool kTok = kSide != kSideWeights, kW = kSide != kSideTokens;
+    constexpr bool kTok = kSide == kSideTokens, kW = kSide == kSideWeights;
     const uint64_t pol_w = g.keep_weights ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
@@ -399,9 +399,9 @@ __device__ __forceinline__ void producer_loop(const GemmMaps& maps, const GemmAr
         }
     }
     if (*s.abort_flag) {
-        // let copies already in flight land before the CTA exits.  (With a
-        // split producer a stage the other side never armed does not complete
-        // although this side's copies landed: one deadline for all stages.)
+        // let copies already in flight land before the CTA exits.  (A stage
+        // the other producer never armed does not complete although this
+        // side's copies landed: one deadline for all stages.)
         const uint64_t t0 = globaltimer();
         for (int i = 0; i < kStages; ++i) {
             if (armed[i] < 0) continue;
@@ -651,17 +651,17 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& g, const GemmSmem&
     }
 }
 
-// All threads: each warp runs its role over the units the CTA's producer draws
-// (kSplit: a block of kThreadsSplit threads, warp 10 the weight-side producer).
-template <class G, bool kSplit = false>
+// All threads (kThreads): each warp runs its role over the units the CTA's
+// token-side producer draws.
+template <class G>
 __device__ __forceinline__ void gemm_roles(const GemmMaps& maps, const GemmArgs& g, const TileView& tv,
                                            const GemmSmem& s, uint32_t tmem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 0) {
-        if (lane == 0) producer_loop<G, kSplit ? kSideTokens : kSideBoth>(maps, g, tv, s);
+        if (lane == 0) producer_loop<G, kSideTokens>(maps, g, tv, s);
     } else if (warp == kWProdWarp) {
-        if (kSplit && lane == 0) producer_loop<G, kSideWeights>(maps, g, tv, s);
+        if (lane == 0) producer_loop<G, kSideWeights>(maps, g, tv, s);
     } else if (warp == 1) {
         mma_loop<G>(g, tv, s, tmem);
     } else {

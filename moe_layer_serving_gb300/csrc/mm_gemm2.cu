@@ -274,7 +274,7 @@ __device__ __forceinline__ void mma2_loop(const GemmArgs& g, int npairs, const G
 
 // Warp 1 of CTA 1: takes the unit numbers out of the ring (one of its
 // consumers), nothing else.
-__device__ __forceinline__ void relay_loop(const GemmArgs& g, int npairs, const GemmSmem& s)
+__device__ __forceinline__ void unit_sink_loop(const GemmArgs& g, int npairs, const GemmSmem& s)
 {
     const int lane = threadIdx.x & 31;
     Unit un;
@@ -290,7 +290,7 @@ __device__ __forceinline__ void relay_loop(const GemmArgs& g, int npairs, const 
     }
 }
 
-__global__ void __launch_bounds__(kThreadsSplit, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm2_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g)
 {
     // the batch went to the one-CTA kernel (launched before this one): every
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreadsSplit, 1)
         if (rank == 0)
             mma2_loop(g, npairs, s, tmem);
         else
-            relay_loop(g, npairs, s);
+            unit_sink_loop(g, npairs, s);
     } else {
         epilogue_loop(g, s, tmem, [&](int u, Unit& un) { return decode2(g, npairs, u, rank, un); },
                       rank == 1 ? peer_addr(s.peer_tmem_empty, 0) : 0u);
@@ -365,7 +365,7 @@ cudaError_t gemm2_prepare(int dev)
     if (dev >= 0 && dev < 64 && g_clusters2[dev] == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2);
-        cfg.blockDim = dim3(kThreadsSplit);
+        cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = kSmem2Bytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -401,7 +401,7 @@ cudaError_t launch_gemm2(const mm_ctx* c, cudaStream_t s, int select)
     const int clusters = g_clusters2[c->dev] < c->sms / 2 ? g_clusters2[c->dev] : c->sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    cfg.blockDim = dim3(kThreadsSplit);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem2Bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

@@ -28,9 +28,9 @@
 namespace mm {
 namespace {
 
-// The GEMM phase runs the split producer (token side in warp 0, weight side in
-// warp 10), so the block has kThreadsSplit threads and every phase uses them.
-constexpr int kSmallThreads = kThreadsSplit;
+// The GEMM phase's roles take kThreads threads (two producer warps, the MMA
+// warp, eight epilogue warps); every other phase uses them all.
+constexpr int kSmallThreads = kThreads;
 constexpr int kSmallWarps = kSmallThreads / 32;
 static_assert(kSmallThreads % 4 == 0, "quant_dispatch_block takes four consecutive lanes per K chunk");
 constexpr int kMaxSmallPairs = kSmallMaxTokens * MM_MAX_TOPK;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     int* t_rows = t_row0 + kMaxSmallTiles;
     int* scal = t_rows + kMaxSmallTiles;            // [0] tiles, [1] rows, [2] [3] tile counts
     static_assert(GeomSmall::kStages >= GeomLarge::kStages, "barriers initialised for the deeper pipeline");
-    const uint32_t tmem = gemm_setup<GeomSmall, true>(s, maps);
+    const uint32_t tmem = gemm_setup<GeomSmall>(s, maps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = a.route.T;
@@ -331,9 +331,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         tv.rows = t_rows;
         tv.ntiles = scal[0];
         if (short_tiles)
-            gemm_roles<GeomSmall, true>(maps, g, tv, s, tmem);
+            gemm_roles<GeomSmall>(maps, g, tv, s, tmem);
         else
-            gemm_roles<GeomLarge, true>(maps, g, tv, s, tmem);
+            gemm_roles<GeomLarge>(maps, g, tv, s, tmem);
     }
     gemm_teardown(tmem);
     if (threadIdx.x == 0) stamp[5] = globaltimer();
