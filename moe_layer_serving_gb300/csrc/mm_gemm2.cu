@@ -16,7 +16,10 @@
 // epilogue is the one-CTA kernel's (SwiGLU pairs gate column c with up column
 // 128 + c in one thread).  An expert with an odd number of tiles leaves the
 // second CTA without a tile in its last pair: that CTA loads only its half of
-// the weights, and its accumulator rows are never read.
+// the weights, and its accumulator rows are never read.  Such pairs cost a
+// whole tile of MMA work each, so by default the large path launches this
+// kernel after the one-CTA kernel and the tile scan picks the one that runs
+// (GemmArgs::select, num_tiles[3]).
 //
 // Roles: warp 0 lane 0 = token-side producer (own token tile and its
 // scales), warp 10 lane 0 = weight-side producer (own weight half and both
@@ -27,8 +30,9 @@
 // which in CTA 1 releases each drained accumulator with one relaxed remote
 // arrive per warp on CTA 0's peer_tmem_empty (relaying through a warp of CTA 1,
 // or arriving from every thread with release semantics, held the pair's MMAs
-// ~1,700 / ~2,000 cycles a unit).  Unit numbers are drawn by CTA 0's token-side producer and
-// handed to CTA 1's, so both run the same sequence.  Every wait is bounded.
+// ~1,700 / ~2,000 cycles a unit).  Unit numbers are drawn by CTA 0's
+// token-side producer and handed to CTA 1's, so both run the same sequence.
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
